@@ -1,0 +1,377 @@
+"""Benchmark of the LM-head contraction + consumer-surface projection on GB300.
+
+Default workload (the decode token-only shape): H [16, 5120] bf16, W [151936, 5120] bf16,
+k = 4 contiguous vocabulary lane shards (S = 37984), surface TOKEN_LOGPROB (argmax token +
+chosen log-prob + logsumexp).  One step = one projection call = the fused GEMM + record
+epilogue kernel followed by the record combine kernel.  W (1.56 GB) is larger than the
+129 MB L2, so every step streams it from HBM and no L2 flush is needed between steps.
+
+Prints one JSON line (rank 0):
+  value       rows/s over the timed steps, inputs resident in HBM, CUDA events around each
+              step on the launching stream, barrier + synchronize on both sides, max over
+              ranks;
+  roofline    the GEMM kernel's algorithmic bytes (W + H read once, outputs written) divided
+              by its own average duration (CUDA events around that kernel inside the timed
+              region), against the measured HBM copy bandwidth;
+  e2e         the same metric through the public C-ABI call with host buffers: each step
+              copies H from pinned host memory, runs the call and reads back token and
+              log-prob, then waits for them;
+  cpu_baseline  the fp64 oracle (plain C, OpenMP over the host cores) on a bounded sample of
+              the same workload (rank 0, N = 1 only).
+``--impl reference`` times that oracle alone as the reference arm.  With N > 1 (torchrun),
+each rank runs its own batch of rows against its own replica of W (weak scaling, no
+collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    "decode16": dict(M=16, d=5120, V=151936, k=4, surface="token_logprob",
+                     desc="decode token-only: H[16,5120] x W[151936,5120] bf16, k=4 shards of 37984, TOKEN + chosen log-prob"),
+    "decode64": dict(M=64, d=4096, V=151936, k=2, surface="full_logits",
+                     desc="decode full-logit: H[64,4096] x W[151936,4096] bf16, k=2, FULL_LOGITS"),
+    "prefill": dict(M=4096, d=6144, V=200064, k=4, surface="token_logprob", targets=True,
+                    desc="prefill scoring: H[4096,6144] x W[200064,6144] bf16, k=4, lse + target log-prob"),
+    "sampling": dict(M=256, d=5120, V=151936, k=4, surface="gumbel_token", T=0.7, seed=1234,
+                     desc="seeded sampling: H[256,5120] x W[151936,5120] bf16, k=4, GUMBEL_TOKEN T=0.7"),
+    "tiny": dict(M=4, d=256, V=4096, k=2, surface="token_logprob",
+                 desc="tiny: H[4,256] x W[4096,256] bf16, k=2"),
+}
+METRIC = "LM-head+projection rows/s; % of HBM GB/s (decode) or bf16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic of the GEMM kernel per launch from an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), with the hash of the kernel source it was taken on; reported as
+# null once the source differs.
+KERNEL_TRAFFIC = {}
+
+
+def kernel_src_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("lmhead.cu", "sb_ptx.cuh", "sb_internal.h"):
+        with open(os.path.join(ROOT, "gemm_epilogue_reduction_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def oracle_rows_per_s(Hb, Wb, k, cfg, rows_per_call, min_seconds, max_calls=None):
+    """Time the oracle (as it stands) on `rows_per_call`-row samples until min_seconds."""
+    import numpy as np
+    import oracle
+    gumbel = cfg["surface"] == "gumbel_token"
+    T = cfg.get("T", 1.0)
+    seed = cfg.get("seed", 0)
+    M = Hb.shape[0]
+    done, calls, t0 = 0, 0, time.perf_counter()
+    while True:
+        r0 = (calls * rows_per_call) % M
+        rows = [(r0 + i) % M for i in range(rows_per_call)]
+        oracle.project(Hb[rows], Wb, k, gumbel=gumbel, temperature=T, seed=seed,
+                       row_ids=np.array(rows))
+        done += rows_per_call
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or (max_calls and calls >= max_calls):
+            return done / el, done, el, oracle.num_threads()
+
+
+def run_reference(args, cfg, world, rank):
+    """The reference arm: the fp64 oracle on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+    import oracle
+    from gemm_epilogue_reduction_gb300 import synth
+    oracle.build()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    H, W = synth.make_hw(cfg["M"], cfg["d"], cfg["V"], seed=0, device=dev)
+    Hb, Wb = synth.bf16_bits(H), synth.bf16_bits(W)
+    del H, W
+    rows_per_step = max(1, min(cfg["M"], 2))
+    gumbel = cfg["surface"] == "gumbel_token"
+    for i in range(args.warmup):
+        oracle.project(Hb[:rows_per_step], Wb, cfg["k"], gumbel=gumbel,
+                       temperature=cfg.get("T", 1.0), seed=cfg.get("seed", 0))
+    times = []
+    for i in range(args.steps):
+        rows = [(i * rows_per_step + j) % cfg["M"] for j in range(rows_per_step)]
+        t0 = time.perf_counter()
+        oracle.project(Hb[rows], Wb, cfg["k"], gumbel=gumbel, temperature=cfg.get("T", 1.0),
+                       seed=cfg.get("seed", 0), row_ids=np.array(rows))
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = rows_per_step * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, **{k: cfg[k] for k in ("M", "d", "V", "k")},
+                   "surface": cfg["surface"], "desc": cfg["desc"]},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"{rows_per_step} of the workload's {cfg['M']} rows per step "
+                                   f"against the full W (fp64 C oracle, OpenMP)"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode16", choices=sorted(WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    cfg = WORKLOADS[args.workload]
+    world, rank, local = dist_env()
+    args.warmup = max(args.warmup, 3)
+
+    if args.impl == "reference":
+        run_reference(args, cfg, world, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import gemm_epilogue_reduction_gb300 as sb
+    from gemm_epilogue_reduction_gb300 import build as sbbuild, synth
+
+    sbbuild.build()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    M, d, V, k = cfg["M"], cfg["d"], cfg["V"], cfg["k"]
+    surface = sb.SURFACES[cfg["surface"]]
+    T = cfg.get("T", 1.0)
+    gseed = cfg.get("seed", 0)
+    # each rank draws its own batch of rows (weak scaling) and the same W
+    H, W = synth.make_hw(M, d, V, seed=0, device="cuda")
+    if rank:
+        H = synth.make_hw(M, d, 1, seed=1000 + rank, device="cuda")[0]
+    targets = synth.make_targets(M, V, seed=1, device="cuda") if cfg.get("targets") else None
+    out, bufs = sb.make_outputs(M, V, k, surface, targets=targets)
+    Tps = sb.sb_tiles_per_shard(M, V, k)
+    stream = torch.cuda.current_stream()
+
+    def step_records():
+        st = sb.sb_lmhead_records(H, W, M, d, V, k, surface, T, gseed, out, stream)
+        if st != sb.SB_OK:
+            raise sb.SbError(st, "sb_lmhead_records")
+
+    def step_combine():
+        st = sb.sb_combine_shard_records(bufs["workspace"], M, k, Tps, surface, T, out, stream)
+        if st != sb.SB_OK:
+            raise sb.SbError(st, "sb_combine_shard_records")
+
+    for _ in range(args.warmup):
+        step_records()
+        step_combine()
+    torch.cuda.synchronize()
+    if sb.sb_last_device_status(out) != sb.SB_OK:
+        raise RuntimeError("device status not OK after warm-up")
+
+    K = args.steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3 * K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_wall = time.perf_counter()
+        for i in range(K):
+            ev[3 * i].record(stream)
+            step_records()
+            ev[3 * i + 1].record(stream)
+            step_combine()
+            ev[3 * i + 2].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    gemm_ms = [ev[3 * i].elapsed_time(ev[3 * i + 1]) for i in range(K)]
+    comb_ms = [ev[3 * i + 1].elapsed_time(ev[3 * i + 2]) for i in range(K)]
+    total_ms = ev[0].elapsed_time(ev[3 * K - 1])
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if sb.sb_last_device_status(out) != sb.SB_OK:
+        raise RuntimeError("device status not OK after the timed region")
+
+    # ---- end to end through the public call, host buffers
+    E = min(args.e2e_steps, K)
+    H_host = H.cpu().pin_memory()
+    tok_host = torch.empty(M, dtype=torch.int32).pin_memory()
+    lp_host = torch.empty(M, dtype=torch.float32).pin_memory()
+    H_dev = torch.empty_like(H)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        H_dev.copy_(H_host, non_blocking=True)
+        st = sb.sb_lmhead_project(H_dev, W, M, d, V, k, surface, T, gseed, out, stream)
+        if st != sb.SB_OK:
+            raise sb.SbError(st, "sb_lmhead_project")
+        tok_host.copy_(bufs["token"], non_blocking=True)
+        lp_host.copy_(bufs["token_logprob"], non_blocking=True)
+        stream.synchronize()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / E
+
+    ms_per_step = total_ms / K
+    value = world * M / (ms_per_step * 1e-3)
+    gemm_avg = sum(gemm_ms) / K
+    comb_avg = sum(comb_ms) / K
+    peaks, peak_src = load_peaks()
+    alg_bytes = V * d * 2 + M * d * 2 + M * 12 + (M * V * 2 if surface == sb.SB_FULL_LOGITS else 0)
+    alg_flops = 2.0 * M * V * d
+    mem_bound = args.workload in ("decode16", "decode64", "tiny", "sampling")
+    achieved_gbs = alg_bytes / (gemm_avg * 1e-3) / 1e9
+    achieved_tfs = alg_flops / (gemm_avg * 1e-3) / 1e12
+    tr = KERNEL_TRAFFIC.get(args.workload)
+    traffic = tr["bytes"] if tr and tr.get("src_sha") == kernel_src_hash() else None
+    if mem_bound:
+        roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
+                "peak_source": f"{peak_src} (HBM copy, burst)", "kernel": "lmhead_kernel",
+                "kernel_ms": gemm_avg, "combine_ms": comb_avg,
+                "algorithmic_bytes": alg_bytes, "tensor_tflops": achieved_tfs}
+    else:
+        roof = {"bound": "tensor", "achieved": achieved_tfs, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved_tfs / peaks["bf16_tflops"], "traffic": traffic,
+                "peak_source": f"{peak_src} (cuBLAS bf16, burst)", "kernel": "lmhead_kernel",
+                "kernel_ms": gemm_avg, "combine_ms": comb_avg, "algorithmic_flops": alg_flops,
+                "hbm_gbs": achieved_gbs}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        Hb, Wb = synth.bf16_bits(H), synth.bf16_bits(W)
+        rows_per_call = max(1, min(M, 4))
+        v, n, el, cores = oracle_rows_per_s(Hb, Wb, k, cfg, rows_per_call, args.cpu_seconds)
+        cpu = {"value": v, "unit": "rows/s", "cores": cores, "kind": "oracle",
+               "sample": f"{n} rows in {el:.1f} s ({rows_per_call}-row calls against the full W)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "M": M, "d": d, "V": V, "k": k,
+                       "surface": cfg["surface"], "desc": cfg["desc"],
+                       "l2": "inputs larger than L2 (W %.2f GB streamed every step)" % (V * d * 2 / 1e9),
+                       "parallelism": "replicas" if world > 1 else "single"},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": M / (e2e_ms * 1e-3) * world, "unit": "rows/s",
+                    "h2d_bytes_per_step": M * d * 2, "d2h_bytes_per_step": M * 8,
+                    "ms_per_step": e2e_ms},
+            "clocks": clocks.summary(),
+            "gpu_launches": 2 * K,
+            "wall_s_timed": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

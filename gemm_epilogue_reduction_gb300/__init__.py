@@ -1,1 +1,191 @@
-"""GB300-native LM-head contraction fused with the consumer-surface projection."""
+"""GB300-native LM-head contraction fused with the consumer-surface projection.
+
+Thin ctypes binding over the C ABI in ``include/sb.h`` (``libsb.so``, built in-tree by
+``gemm_epilogue_reduction_gb300.build``). The functions named ``sb_*`` mirror the C entry
+points one to one and only marshal arguments: every step of the path runs in the CUDA
+kernels. ``project`` is a convenience wrapper that allocates the outputs and workspace with
+torch (the caller-owned memory of the C ABI) and raises on a non-OK status.
+
+There is no CPU fallback: if ``libsb.so`` is missing or cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+SB_TOKEN, SB_TOKEN_LOGPROB, SB_FULL_LOGITS, SB_GUMBEL_TOKEN = 0, 1, 2, 3
+SURFACES = {"token": SB_TOKEN, "token_logprob": SB_TOKEN_LOGPROB,
+            "full_logits": SB_FULL_LOGITS, "gumbel_token": SB_GUMBEL_TOKEN}
+SB_OK = 0
+SB_ERR_INVALID_ARG = 1
+SB_ERR_UNSUPPORTED = 2
+SB_ERR_ALIGNMENT = 3
+SB_ERR_WORKSPACE_TOO_SMALL = 4
+SB_ERR_CUDA = 5
+SB_ERR_DEVICE_TIMEOUT = 6
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libsb.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class SbError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: status {status} ({sb_status_string(status)})")
+        self.status = status
+
+
+class sb_outputs(ctypes.Structure):
+    _fields_ = [("token", ctypes.c_void_p), ("token_logprob", ctypes.c_void_p),
+                ("lse", ctypes.c_void_p), ("logits_bf16", ctypes.c_void_p),
+                ("target_ids", ctypes.c_void_p), ("target_logprob", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
+def lib():
+    """The loaded libsb.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libsb.so not found at {LIB_PATH}: build it first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i64, i32, u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64
+        L.sb_workspace_bytes.argtypes = [i64, i64, i32, i32]
+        L.sb_workspace_bytes.restype = ctypes.c_size_t
+        L.sb_tiles_per_shard.argtypes = [i64, i64, i32]
+        L.sb_tiles_per_shard.restype = i32
+        L.sb_lmhead_project.argtypes = [P, P, i64, i64, i64, i32, i32, ctypes.c_float, u64,
+                                        ctypes.POINTER(sb_outputs), P]
+        L.sb_lmhead_project.restype = i32
+        L.sb_lmhead_records.argtypes = L.sb_lmhead_project.argtypes
+        L.sb_lmhead_records.restype = i32
+        L.sb_combine_shard_records.argtypes = [P, i64, i32, i32, i32, ctypes.c_float,
+                                               ctypes.POINTER(sb_outputs), P]
+        L.sb_combine_shard_records.restype = i32
+        L.sb_last_device_status.argtypes = [ctypes.POINTER(sb_outputs)]
+        L.sb_last_device_status.restype = i32
+        L.sb_status_string.argtypes = [i32]
+        L.sb_status_string.restype = ctypes.c_char_p
+        L.sb_device_info.argtypes = [ctypes.POINTER(i32), ctypes.POINTER(i32)]
+        L.sb_device_info.restype = i32
+        L.sb_debug_configure.argtypes = [i32, u64]
+        L.sb_debug_configure.restype = i32
+        _lib = L
+        return L
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+# ------------------------------------------------------------------ C entry points
+def sb_workspace_bytes(M: int, V: int, k: int, surface: int) -> int:
+    return int(lib().sb_workspace_bytes(M, V, k, surface))
+
+
+def sb_tiles_per_shard(M: int, V: int, k: int) -> int:
+    return int(lib().sb_tiles_per_shard(M, V, k))
+
+
+def sb_lmhead_project(H, W, M, d, V, k, surface, temperature, seed, out: sb_outputs,
+                      stream=None) -> int:
+    return int(lib().sb_lmhead_project(_ptr(H), _ptr(W), M, d, V, k, surface,
+                                       float(temperature), seed & (2**64 - 1),
+                                       ctypes.byref(out), _stream(stream)))
+
+
+def sb_lmhead_records(H, W, M, d, V, k, surface, temperature, seed, out: sb_outputs,
+                      stream=None) -> int:
+    return int(lib().sb_lmhead_records(_ptr(H), _ptr(W), M, d, V, k, surface,
+                                       float(temperature), seed & (2**64 - 1),
+                                       ctypes.byref(out), _stream(stream)))
+
+
+def sb_combine_shard_records(workspace, M, k, tiles_per_shard, surface, temperature,
+                             out: sb_outputs, stream=None) -> int:
+    return int(lib().sb_combine_shard_records(_ptr(workspace), M, k, tiles_per_shard,
+                                              surface, float(temperature),
+                                              ctypes.byref(out), _stream(stream)))
+
+
+def sb_last_device_status(out: sb_outputs) -> int:
+    return int(lib().sb_last_device_status(ctypes.byref(out)))
+
+
+def sb_status_string(status: int) -> str:
+    return lib().sb_status_string(status).decode()
+
+
+def sb_device_info():
+    n, cc = ctypes.c_int32(0), ctypes.c_int32(0)
+    if lib().sb_device_info(ctypes.byref(n), ctypes.byref(cc)) != 0:
+        return None
+    return n.value, cc.value
+
+
+def sb_debug_configure(stall_epilogue: bool, wait_limit_ns: int) -> int:
+    return int(lib().sb_debug_configure(1 if stall_epilogue else 0, int(wait_limit_ns)))
+
+
+# ------------------------------------------------------------------ convenience wrapper
+def make_outputs(M: int, V: int, k: int, surface: int, *, device="cuda", lse=True,
+                 logprob=True, targets=None, workspace=None):
+    """Allocate the caller-owned buffers of one call with torch; returns (sb_outputs, dict)."""
+    import torch
+    bufs = {"token": torch.empty(M, dtype=torch.int32, device=device)}
+    if logprob or surface in (SB_TOKEN_LOGPROB, SB_GUMBEL_TOKEN):
+        bufs["token_logprob"] = torch.empty(M, dtype=torch.float32, device=device)
+    if lse:
+        bufs["lse"] = torch.empty(M, dtype=torch.float32, device=device)
+    if surface == SB_FULL_LOGITS:
+        bufs["logits"] = torch.empty(M, V, dtype=torch.bfloat16, device=device)
+    if targets is not None:
+        bufs["target_ids"] = targets
+        bufs["target_logprob"] = torch.empty(M, dtype=torch.float32, device=device)
+    nbytes = sb_workspace_bytes(M, V, k, surface)
+    if nbytes == 0:
+        raise SbError(SB_ERR_INVALID_ARG, "sb_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    bufs["workspace"] = workspace
+    out = sb_outputs(_ptr(bufs["token"]), _ptr(bufs.get("token_logprob")), _ptr(bufs.get("lse")),
+                     _ptr(bufs.get("logits")), _ptr(bufs.get("target_ids")),
+                     _ptr(bufs.get("target_logprob")), _ptr(workspace),
+                     workspace.numel() * workspace.element_size())
+    return out, bufs
+
+
+def project(H, W, k: int, surface: int = SB_TOKEN_LOGPROB, *, temperature: float = 1.0,
+            seed: int = 0, targets=None, stream=None, lse=True, logprob=True, workspace=None):
+    """Run one projection call on torch CUDA tensors H [M, d] and W [V, d] (bf16).
+
+    Returns the dict of output tensors (token, token_logprob, lse, logits, target_logprob,
+    workspace, as requested). Asynchronous on ``stream``; raises SbError on a bad status."""
+    M, d = H.shape
+    V = W.shape[0]
+    out, bufs = make_outputs(M, V, k, surface, device=H.device, lse=lse, logprob=logprob,
+                             targets=targets, workspace=workspace)
+    st = sb_lmhead_project(H, W, M, d, V, k, surface, temperature, seed, out, stream)
+    if st != SB_OK:
+        raise SbError(st, "sb_lmhead_project")
+    bufs["_outputs"] = out
+    return bufs

@@ -1,0 +1,592 @@
+// lmhead.cu -- the fused output-head GEMM + projection-record epilogue for sm_103a.
+//
+// One persistent, warp-specialised kernel computes z = H·Wᵀ tile by tile on the
+// 5th-generation tensor cores and reduces each tile straight out of TMEM into compact
+// per-(row, lane shard, tile) records (max, lowest argmax, sum of exp), so the token
+// surface never writes logits to HBM ("SemBridge: Compiling Consumer Observations into
+// Cross-Stack Communication Plans", Section 5.2 and Figure 1: source projection applies
+// the deterministic argmax where the logits are produced).  The full-logit surface
+// additionally writes bf16 logits in shard-to-full (global column) layout.
+//
+// Structure (the warp roles and TMEM epilogue of the "01 · 通算融合" note on Blackwell
+// SM100 GEMMs, sections 2 and 5.1: TMA producer, MMA issuer, epilogue warps; full-K
+// accumulation before any epilogue work):
+//   warp 0      one lane issues TMA loads of 64-wide K slices of both operands into a
+//               ring of shared-memory stages (128-byte swizzle);
+//   warp 1      owns the TMEM allocation; one lane issues tcgen05.mma (M = 128,
+//               bf16 x bf16 -> fp32) into one of two TMEM accumulators and commits
+//               stage releases and "accumulator full" to mbarriers;
+//   warps 2-5   the epilogue: tcgen05.ld of the finished accumulator (warp w reads TMEM
+//               lanes 32*(w%4) .. +31), mask columns outside the tile's shard, fold the
+//               projection record, release the accumulator to the MMA warp.
+// Two tile orientations share the pipeline:
+//   vocab mode (M <= 256, decode and sampling): A = 128 rows of W (vocabulary), B = all
+//               M rows of H (UMMA N = M rounded up to 16).  TMEM lane = vocabulary
+//               column; the epilogue reduces across lanes with warp reductions.
+//   rows mode  (M > 256, prefill scoring): A = 128 rows of H, B = 256 rows of W.
+//               TMEM lane = row of H; each epilogue thread folds its row serially.
+// Vocabulary tiles never cross a lane-shard boundary: tile t of shard s starts at
+// s*S + t*TV and is masked at (s+1)*S, so each record belongs to one shard.
+//
+// Every mbarrier wait is bounded (a time limit read from %globaltimer); a wait that runs
+// out records SB_ERR_DEVICE_TIMEOUT in the workspace status word, raises a CTA-wide abort
+// flag, and every role then drains its own in-flight TMA copies and MMAs before the TMEM
+// is freed and the CTA exits.
+#include <cfloat>
+#include <climits>
+#include <cuda_bf16.h>
+
+#include "sb_internal.h"
+#include "sb_ptx.cuh"
+
+namespace sb {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kStageBytesA = kTileA * kBlockK * 2;  // 16 KB
+constexpr uint32_t kTimeoutCode = 6;                      // SB_ERR_DEVICE_TIMEOUT
+
+struct SmemLayout {
+    uint32_t a_off, b_off, bar_off, misc_off, tgt_off, scratch_off, total;
+};
+
+__host__ __device__ inline SmemLayout make_layout(int nb, int stages, bool vocab, int flags) {
+    SmemLayout L;
+    uint32_t off = 0;
+    L.a_off = off;
+    off += stages * kStageBytesA;
+    L.b_off = off;
+    off += stages * nb * 128;
+    L.bar_off = off;
+    off += (2 * kMaxStages + 8) * 8;
+    L.misc_off = off;
+    off += 16;
+    L.tgt_off = off;
+    off += vocab ? kMaxVocabModeRows * 4 : 0;
+    L.scratch_off = off;
+    off += vocab ? 4 * nb * ((flags & kFlagGumbel) ? 24 : 12) : 0;
+    L.total = off + 1024;  // slack to align the base to 1024 bytes
+    return L;
+}
+
+struct TileCoord {
+    int s, t, v0, v_end, m0, a_row, b_row;
+};
+
+template <bool VOCAB>
+__device__ __forceinline__ TileCoord tile_coord(const GemmParams &p, int tile) {
+    TileCoord c;
+    const int vt = VOCAB ? tile : tile / p.m_tiles;
+    const int mt = VOCAB ? 0 : tile % p.m_tiles;
+    c.s = vt / p.T;
+    c.t = vt - c.s * p.T;
+    c.v0 = c.s * p.S + c.t * p.tv;
+    c.v_end = min(c.v0 + p.tv, (c.s + 1) * p.S);
+    c.m0 = mt * kTileA;
+    c.a_row = VOCAB ? c.v0 : c.m0;
+    c.b_row = VOCAB ? 0 : c.v0;
+    return c;
+}
+
+__device__ __noinline__ void raise_timeout(const GemmParams &p, volatile int *abort_flag) {
+    *abort_flag = 1;
+    atomicMax(p.ws.status, (static_cast<unsigned long long>(p.epoch) << 32) | kTimeoutCode);
+}
+
+// Bounded wait on an mbarrier phase.  Returns false when the CTA is aborting (another
+// role gave up) or when this wait itself runs out of time.
+__device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                      const GemmParams &p) {
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test(bar, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > p.timeout_ns) {
+                raise_timeout(p, abort_flag);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait used while draining: ignores the abort flag (the copies or MMAs being
+// waited for complete on their own), but still gives up after the time limit.
+__device__ __forceinline__ void bwait_drain(uint64_t *bar, uint32_t parity,
+                                            volatile int *abort_flag, const GemmParams &p) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_test(bar, parity)) return;
+        if ((i & 63u) == 63u && globaltimer_ns() - t0 > p.timeout_ns) {
+            raise_timeout(p, abort_flag);
+            return;
+        }
+    }
+}
+
+__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Named-barrier vote over the 128 epilogue threads: true if any thread passes true.
+__device__ __forceinline__ bool epi_vote_any(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred))
+        : "memory");
+    return r != 0;
+}
+
+// Counter-based Gumbel noise: SplitMix64 (Steele, Lea and Flood, OOPSLA 2014) at stream
+// index n of the stream seeded with `seed` (state seed + (n + 1) * golden increment,
+// then the finaliser), top 24 bits as u in [0, 1), g = -log(-log u) in fp32.
+__device__ __forceinline__ float gumbel_noise(unsigned long long seed, unsigned long long n) {
+    unsigned long long x = seed + (n + 1ull) * 0x9E3779B97F4A7C15ull;
+    x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
+    x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
+    x ^= x >> 31;
+    const float u = static_cast<float>(static_cast<uint32_t>(x >> 40)) * 5.9604644775390625e-8f;
+    return -logf(-logf(u));
+}
+
+__device__ __forceinline__ uint16_t bf16_bits_rn(float z) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(z));
+}
+
+// ------------------------------------------------------------------ epilogue, vocab mode
+// Thread (warp quadrant q, lane) holds vocabulary column v = v0 + 32q + lane for every row
+// (TMEM columns).  Per row: warp max / lowest argmax / sum of exp with warp reductions,
+// then the four warps' partial records merge in quadrant order through shared memory.
+template <bool GUMBEL, bool FULL>
+__device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCoord &c,
+                                               uint32_t taddr, uint64_t *tempty_b, int q,
+                                               int lane, const int32_t *tgt_s,
+                                               float *scratch) {
+    const int nb = p.nb;
+    const int v = c.v0 + 32 * q + lane;
+    const bool valid = v < c.v_end;
+    const bool has_t = (p.flags & kFlagTargets) != 0;
+    float *sc_m = scratch;
+    int *sc_i = reinterpret_cast<int *>(scratch + 4 * nb);
+    float *sc_s = scratch + 8 * nb;
+    float *sc_gk = scratch + 12 * nb;
+    int *sc_gi = reinterpret_cast<int *>(scratch + 16 * nb);
+    float *sc_gz = scratch + 20 * nb;
+
+    for (int c0 = 0; c0 < nb; c0 += 32) {
+        uint32_t raw[32];
+        const int cw = min(32, nb - c0);
+        if (cw == 32)
+            tmem_ld32x32b_x32(taddr + c0, raw);
+        else
+            tmem_ld32x32b_x16(taddr + c0, raw);
+        if (c0 + 32 >= nb) {  // last TMEM read of this tile: hand the accumulator back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_b);
+        }
+        float my_m = -INFINITY, my_s = 0.f, my_gk = -INFINITY, my_gz = 0.f;
+        int my_i = INT_MAX, my_gi = INT_MAX;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int row = c0 + j;
+            if (j >= cw || row >= p.M) break;
+            const float z = __uint_as_float(raw[j]);
+            const float y = valid ? (GUMBEL ? z * p.inv_t : z) : -INFINITY;
+            const uint32_t oy = float_to_ordered(y);
+            const uint32_t om = __reduce_max_sync(0xFFFFFFFFu, oy);
+            const float wm = ordered_to_float(om);
+            const int wi = __reduce_min_sync(0xFFFFFFFFu, (valid && oy == om) ? v : INT_MAX);
+            float ws = valid ? ex2_approx(fmaf(y, kLog2e, -wm * kLog2e)) : 0.f;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ws += __shfl_xor_sync(0xFFFFFFFFu, ws, off);
+            if (GUMBEL) {
+                const float g = gumbel_noise(
+                    p.seed, static_cast<unsigned long long>(row) * static_cast<unsigned>(p.V) +
+                                static_cast<unsigned>(v));
+                const float key = valid ? y + g : -INFINITY;
+                const uint32_t ok = float_to_ordered(key);
+                const uint32_t okm = __reduce_max_sync(0xFFFFFFFFu, ok);
+                const int gi = __reduce_min_sync(0xFFFFFFFFu, (valid && ok == okm) ? v : INT_MAX);
+                const int src = (gi == INT_MAX) ? 0 : (gi - (c.v0 + 32 * q));
+                const float gz = __shfl_sync(0xFFFFFFFFu, z, src & 31);
+                if (lane == j) {
+                    my_gk = ordered_to_float(okm);
+                    my_gi = gi;
+                    my_gz = gz;
+                }
+            }
+            if (FULL && valid) p.logits[static_cast<size_t>(row) * p.V + v] = bf16_bits_rn(z);
+            if (has_t && valid && tgt_s[row] == v) p.ws.tz[row] = z;
+            if (lane == j) {
+                my_m = wm;
+                my_i = wi;
+                my_s = ws;
+            }
+        }
+        if (lane < cw && c0 + lane < p.M) {
+            const int o = q * nb + c0 + lane;
+            sc_m[o] = my_m;
+            sc_i[o] = my_i;
+            sc_s[o] = my_s;
+            if (GUMBEL) {
+                sc_gk[o] = my_gk;
+                sc_gi[o] = my_gi;
+                sc_gz[o] = my_gz;
+            }
+        }
+    }
+    epi_bar_sync();
+    const int te = threadIdx.x - 64;
+    for (int row = te; row < p.M; row += 128) {
+        float m = -INFINITY;
+        int idx = INT_MAX;
+        for (int w = 0; w < 4; ++w) {
+            const float mw = sc_m[w * nb + row];
+            const int iw = sc_i[w * nb + row];
+            if (mw > m || (mw == m && iw < idx)) {
+                m = mw;
+                idx = iw;
+            }
+        }
+        float s = 0.f;
+        for (int w = 0; w < 4; ++w) {
+            const float mw = sc_m[w * nb + row];
+            if (mw != -INFINITY) s += sc_s[w * nb + row] * ex2_approx((mw - m) * kLog2e);
+        }
+        const size_t ri = (static_cast<size_t>(row) * p.k + c.s) * p.T + c.t;
+        p.ws.m[ri] = m;
+        p.ws.idx[ri] = idx;
+        p.ws.s[ri] = s;
+        if (GUMBEL) {
+            float gk = -INFINITY, gz = 0.f;
+            int gi = INT_MAX;
+            for (int w = 0; w < 4; ++w) {
+                const float kw = sc_gk[w * nb + row];
+                const int iw = sc_gi[w * nb + row];
+                if (kw > gk || (kw == gk && iw < gi)) {
+                    gk = kw;
+                    gi = iw;
+                    gz = sc_gz[w * nb + row];
+                }
+            }
+            p.ws.gk[ri] = gk;
+            p.ws.gi[ri] = gi;
+            p.ws.gz[ri] = gz;
+        }
+    }
+    epi_bar_sync();
+}
+
+// ------------------------------------------------------------------ epilogue, rows mode
+// Thread (quadrant q, lane) owns row m0 + 32q + lane and walks the tile's 256 columns in
+// chunks of 32: chunk max and first argmax, online rescale of the running sum, then the
+// sum of exp against the running max.
+template <bool GUMBEL, bool FULL>
+__device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoord &c,
+                                              uint32_t taddr, uint64_t *tempty_b, int q,
+                                              int lane) {
+    const int row = c.m0 + 32 * q + lane;
+    const bool rv = row < p.M;
+    const int tgt = ((p.flags & kFlagTargets) && rv) ? __ldg(p.targets + row) : -1;
+    float rm = -INFINITY, rs = 0.f, gk = -INFINITY, gz = 0.f;
+    int ri = INT_MAX, gi = INT_MAX;
+    constexpr int kChunks = kRowsTileN / 32;
+#pragma unroll 1
+    for (int ch = 0; ch < kChunks; ++ch) {
+        uint32_t raw[32];
+        tmem_ld32x32b_x32(taddr + ch * 32, raw);
+        if (ch == kChunks - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_b);
+        }
+        const int cb = c.v0 + ch * 32;
+        const int nval = min(32, c.v_end - cb);
+        if (nval <= 0) continue;
+        float y[32];
+        float cm = -INFINITY;
+        int cj = 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float z = __uint_as_float(raw[j]);
+            y[j] = (j < nval) ? (GUMBEL ? z * p.inv_t : z) : -INFINITY;
+            if (y[j] > cm) {
+                cm = y[j];
+                cj = j;
+            }
+        }
+        if (cm > rm) {
+            rs *= ex2_approx((rm - cm) * kLog2e);
+            rm = cm;
+            ri = cb + cj;
+        }
+        const float mb = rm * kLog2e;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) rs += ex2_approx(fmaf(y[j], kLog2e, -mb));
+        if (GUMBEL && rv) {
+            const unsigned long long nbase =
+                static_cast<unsigned long long>(row) * static_cast<unsigned>(p.V) +
+                static_cast<unsigned>(cb);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                if (j < nval) {
+                    const float key = y[j] + gumbel_noise(p.seed, nbase + j);
+                    if (key > gk) {
+                        gk = key;
+                        gi = cb + j;
+                        gz = __uint_as_float(raw[j]);
+                    }
+                }
+            }
+        }
+        if (tgt >= cb && tgt < cb + nval) {
+            float tzv = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (j == tgt - cb) tzv = __uint_as_float(raw[j]);
+            p.ws.tz[row] = tzv;
+        }
+        if (FULL && rv) {
+            uint16_t *dst = p.logits + static_cast<size_t>(row) * p.V + cb;
+            if (nval == 32 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    pk[j] = static_cast<uint32_t>(bf16_bits_rn(__uint_as_float(raw[2 * j]))) |
+                            (static_cast<uint32_t>(bf16_bits_rn(__uint_as_float(raw[2 * j + 1])))
+                             << 16);
+                uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (j < nval) dst[j] = bf16_bits_rn(__uint_as_float(raw[j]));
+            }
+        }
+    }
+    if (rv) {
+        const size_t o = (static_cast<size_t>(row) * p.k + c.s) * p.T + c.t;
+        p.ws.m[o] = rm;
+        p.ws.idx[o] = ri;
+        p.ws.s[o] = rs;
+        if (GUMBEL) {
+            p.ws.gk[o] = gk;
+            p.ws.gi[o] = gi;
+            p.ws.gz[o] = gz;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ the kernel
+template <bool VOCAB, bool GUMBEL, bool FULL>
+__global__ void __launch_bounds__(kThreads, 1)
+    lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const GemmParams p, const uint32_t tmem_cols) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    const SmemLayout L = make_layout(p.nb, p.stages, VOCAB, p.flags);
+    uint8_t *sA = smem + L.a_off;
+    uint8_t *sB = smem + L.b_off;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + kMaxStages;
+    uint64_t *tfull = bars + 2 * kMaxStages;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint64_t *stall = drain + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.misc_off);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.misc_off + 4);
+    int32_t *tgt_s = reinterpret_cast<int32_t *>(smem + L.tgt_off);
+    float *scratch = reinterpret_cast<float *>(smem + L.scratch_off);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t b_stage_bytes = static_cast<uint32_t>(p.nb) * 128u;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < p.stages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], 4);
+        }
+        mbar_init(drain, 1);
+        mbar_init(stall, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        if (blockIdx.x == 0) *p.ws.epoch = p.epoch;
+    }
+    if (VOCAB && (p.flags & kFlagTargets))
+        for (int i = threadIdx.x; i < p.M; i += blockDim.x) tgt_s[i] = p.targets[i];
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (one lane)
+        if (lane == 0) {
+            const uint64_t pol_a = VOCAB ? policy_evict_first() : policy_evict_last();
+            const uint64_t pol_b = VOCAB ? policy_evict_last() : policy_evict_normal();
+            int stage = 0;
+            uint32_t phase = 0, issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+                const TileCoord c = tile_coord<VOCAB>(p, tile);
+                for (int kb = 0; kb < p.kblocks; ++kb) {
+                    if (!bwait(&empty[stage], phase ^ 1u, abort_flag, p)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], kStageBytesA + b_stage_bytes);
+                    tma_load_2d(sA + stage * kStageBytesA, &tmA, &full[stage], kb * kBlockK,
+                                c.a_row, pol_a);
+                    tma_load_2d(sB + stage * b_stage_bytes, &tmB, &full[stage], kb * kBlockK,
+                                c.b_row, pol_b);
+                    ++issued;
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Drain: the last `stages` issues may still be landing (only possible after an
+            // abort; on the normal path the MMA warp consumed every one of them).
+            const uint32_t n = issued < static_cast<uint32_t>(p.stages) ? issued : p.stages;
+            for (uint32_t i = issued - n; i < issued; ++i)
+                bwait_drain(&full[i % p.stages], (i / p.stages) & 1u, abort_flag, p);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (one lane)
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kTileA, p.nb);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true, any = false;
+            int it = 0;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+                const int b = it & 1;
+                const uint32_t tph = (it >> 1) & 1;
+                if (!bwait(&tempty[b], tph ^ 1u, abort_flag, p)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * p.nb);
+                for (int kb = 0; kb < p.kblocks; ++kb) {
+                    if (!bwait(&full[stage], phase, abort_flag, p)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * kStageBytesA));
+                    const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * b_stage_bytes));
+#pragma unroll
+                    for (int ks = 0; ks < kBlockK / 16; ++ks)
+                        umma_bf16(d_tmem, adesc + 2u * ks, bdesc + 2u * ks, idesc,
+                                  (kb | ks) != 0 ? 1u : 0u);
+                    umma_commit(&empty[stage]);
+                    any = true;
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) umma_commit(&tfull[b]);
+            }
+            if (any) {  // wait until every MMA this thread issued has completed
+                umma_commit(drain);
+                bwait_drain(drain, 0, abort_flag, p);
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue warps 2..5
+        const int q = warp & 3;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+            const int b = it & 1;
+            const uint32_t tph = (it >> 1) & 1;
+            bool ok;
+            if (p.debug_stall)
+                ok = bwait(stall, 0, abort_flag, p);  // nothing ever arrives here
+            else
+                ok = bwait(&tfull[b], tph, abort_flag, p);
+            if (epi_vote_any(!ok)) break;
+            tc_fence_after();
+            const TileCoord c = tile_coord<VOCAB>(p, tile);
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * p.nb);
+            if (VOCAB)
+                epilogue_vocab<GUMBEL, FULL>(p, c, taddr, &tempty[b], q, lane, tgt_s, scratch);
+            else
+                epilogue_rows<GUMBEL, FULL>(p, c, taddr, &tempty[b], q, lane);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, tmem_cols);
+    }
+}
+
+template <bool VOCAB, bool GUMBEL, bool FULL>
+cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p,
+                     int grid, size_t smem, cudaStream_t stream) {
+    auto kern = lmhead_kernel<VOCAB, GUMBEL, FULL>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    uint32_t cols = 512;
+    if (VOCAB) {
+        cols = 32;
+        while (cols < static_cast<uint32_t>(2 * p.nb)) cols <<= 1;
+    }
+    kern<<<grid, kThreads, smem, stream>>>(tmA, tmB, p, cols);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t lmhead_smem_bytes(int nb, int stages, bool vocab_mode, int flags) {
+    return make_layout(nb, stages, vocab_mode, flags).total;
+}
+
+int lmhead_max_stages(int nb, bool vocab_mode, int flags) {
+    int s = kMaxStages;
+    while (s > 1 && make_layout(nb, s, vocab_mode, flags).total > kSmemLimit) --s;
+    return s;
+}
+
+cudaError_t launch_lmhead(bool vocab_mode, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                          const GemmParams &p, int grid, size_t smem, cudaStream_t stream) {
+    const bool g = (p.flags & kFlagGumbel) != 0;
+    const bool f = (p.flags & kFlagFull) != 0;
+    if (vocab_mode) {
+        if (g) return f ? launch_t<true, true, true>(tmA, tmB, p, grid, smem, stream)
+                        : launch_t<true, true, false>(tmA, tmB, p, grid, smem, stream);
+        return f ? launch_t<true, false, true>(tmA, tmB, p, grid, smem, stream)
+                 : launch_t<true, false, false>(tmA, tmB, p, grid, smem, stream);
+    }
+    if (g) return f ? launch_t<false, true, true>(tmA, tmB, p, grid, smem, stream)
+                    : launch_t<false, true, false>(tmA, tmB, p, grid, smem, stream);
+    return f ? launch_t<false, false, true>(tmA, tmB, p, grid, smem, stream)
+             : launch_t<false, false, false>(tmA, tmB, p, grid, smem, stream);
+}
+
+}  // namespace sb

@@ -1,0 +1,330 @@
+// sb_api.cu -- host side of the libsb C ABI: argument validation, workspace layout,
+// TMA tensor-map encoding, variant choice and kernel launches on the caller's stream.
+// The library allocates no device memory and never synchronises.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "sb.h"
+#include "sb_internal.h"
+
+namespace {
+using namespace sb;
+
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
+
+std::atomic<uint32_t> g_epoch{0x5B000000u};
+std::atomic<int> g_debug_stall{0};
+std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
+
+size_t al256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+struct WsLayout {
+    size_t m, idx, s, gk, gi, gz, tz, total;
+};
+
+WsLayout ws_layout(int64_t M, int32_t k, int32_t T, bool gumbel) {
+    const size_t n = static_cast<size_t>(M) * k * T;
+    WsLayout L{};
+    size_t off = 256;
+    L.m = off;
+    off += al256(4 * n);
+    L.idx = off;
+    off += al256(4 * n);
+    L.s = off;
+    off += al256(4 * n);
+    if (gumbel) {
+        L.gk = off;
+        off += al256(4 * n);
+        L.gi = off;
+        off += al256(4 * n);
+        L.gz = off;
+        off += al256(4 * n);
+    }
+    L.tz = off;
+    off += al256(4 * static_cast<size_t>(M));
+    L.total = off;
+    return L;
+}
+
+Workspace ws_views(void *base, const WsLayout &L, bool gumbel) {
+    uint8_t *b = static_cast<uint8_t *>(base);
+    Workspace w{};
+    w.epoch = reinterpret_cast<uint32_t *>(b);
+    w.status = reinterpret_cast<unsigned long long *>(b + 8);
+    w.m = reinterpret_cast<float *>(b + L.m);
+    w.idx = reinterpret_cast<int32_t *>(b + L.idx);
+    w.s = reinterpret_cast<float *>(b + L.s);
+    if (gumbel) {
+        w.gk = reinterpret_cast<float *>(b + L.gk);
+        w.gi = reinterpret_cast<int32_t *>(b + L.gi);
+        w.gz = reinterpret_cast<float *>(b + L.gz);
+    }
+    w.tz = reinterpret_cast<float *>(b + L.tz);
+    return w;
+}
+
+bool shape_ok(int64_t M, int64_t V, int32_t k) {
+    return M >= 1 && M <= (int64_t(1) << 30) && V >= 1 && V < (int64_t(1) << 31) && k >= 1 &&
+           V % k == 0;
+}
+
+bool vocab_mode(int64_t M) { return M <= kMaxVocabModeRows; }
+
+int32_t tiles_per_shard(int64_t M, int64_t V, int32_t k) {
+    const int64_t S = V / k;
+    const int64_t tv = vocab_mode(M) ? kVocabTileV : kRowsTileN;
+    return static_cast<int32_t>((S + tv - 1) / tv);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D map over a row-major bf16 matrix [rows, d]: boxes of 64 x box_rows, 128-byte swizzle,
+// out-of-range elements read as zero.
+bool make_map(CUtensorMap *tm, const void *base, int64_t rows, int64_t d, int box_rows) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t es[2] = {1, 1};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct DevInfo {
+    int sms = 0, cc = 0;
+};
+
+int32_t current_device(DevInfo *out) {
+    static DevInfo cache[64];
+    static std::atomic<uint64_t> known{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SB_ERR_CUDA;
+    if (dev < 64 && (known.load() >> dev) & 1) {
+        *out = cache[dev];
+    } else {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SB_ERR_CUDA;
+        out->sms = sms;
+        out->cc = major * 10 + minor;
+        if (dev < 64) {
+            cache[dev] = *out;
+            known.fetch_or(uint64_t(1) << dev);
+        }
+    }
+    return out->cc == 103 ? SB_OK : SB_ERR_UNSUPPORTED;
+}
+
+int32_t check_outputs(const sb_outputs *out, int32_t surface, bool need_ws) {
+    if (!out || !out->token) return SB_ERR_INVALID_ARG;
+    if ((surface == SB_TOKEN_LOGPROB || surface == SB_GUMBEL_TOKEN) && !out->token_logprob)
+        return SB_ERR_INVALID_ARG;
+    if (surface == SB_FULL_LOGITS && !out->logits_bf16) return SB_ERR_INVALID_ARG;
+    if ((out->target_ids == nullptr) != (out->target_logprob == nullptr)) return SB_ERR_INVALID_ARG;
+    if (need_ws && !out->workspace) return SB_ERR_INVALID_ARG;
+    if (!aligned(out->token, 4) || !aligned(out->token_logprob, 4) || !aligned(out->lse, 4) ||
+        !aligned(out->target_ids, 4) || !aligned(out->target_logprob, 4) ||
+        !aligned(out->logits_bf16, 16) || !aligned(out->workspace, 256))
+        return SB_ERR_ALIGNMENT;
+    return SB_OK;
+}
+
+CombineParams combine_params(const sb_outputs *out, const Workspace &w, int64_t M, int32_t k,
+                             int32_t T, int flags, float inv_t) {
+    CombineParams c{};
+    c.M = static_cast<int>(M);
+    c.k = k;
+    c.T = T;
+    c.flags = flags;
+    c.inv_t = inv_t;
+    c.ws = w;
+    c.token = out->token;
+    c.token_logprob = out->token_logprob;
+    c.lse = out->lse;
+    c.target_logprob = out->target_ids ? out->target_logprob : nullptr;
+    return c;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t sb_workspace_bytes(int64_t M, int64_t V, int32_t k, int32_t surface) {
+    if (!shape_ok(M, V, k) || surface < SB_TOKEN || surface > SB_GUMBEL_TOKEN) return 0;
+    return ws_layout(M, k, tiles_per_shard(M, V, k), surface == SB_GUMBEL_TOKEN).total;
+}
+
+int32_t sb_tiles_per_shard(int64_t M, int64_t V, int32_t k) {
+    if (!shape_ok(M, V, k)) return -1;
+    return tiles_per_shard(M, V, k);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Validates, then enqueues the fused GEMM + record epilogue and, when `with_combine`, the
+// record combine.
+int32_t enqueue(const void *H, const void *W, int64_t M, int64_t d, int64_t V, int32_t k,
+                int32_t surface, float temperature, uint64_t seed, const sb_outputs *out,
+                void *stream, bool with_combine) {
+    if (!H || !W || !shape_ok(M, V, k) || d < 8 || d > (int64_t(1) << 24) ||
+        surface < SB_TOKEN || surface > SB_GUMBEL_TOKEN)
+        return SB_ERR_INVALID_ARG;
+    const bool gumbel = surface == SB_GUMBEL_TOKEN;
+    if (gumbel && !(std::isfinite(temperature) && temperature > 0.f)) return SB_ERR_INVALID_ARG;
+    if (int32_t e = check_outputs(out, surface, true)) return e;
+    if (d % 8 != 0 || !aligned(H, 16) || !aligned(W, 16)) return SB_ERR_ALIGNMENT;
+    const int32_t T = tiles_per_shard(M, V, k);
+    const WsLayout L = ws_layout(M, k, T, gumbel);
+    if (out->workspace_bytes < L.total) return SB_ERR_WORKSPACE_TOO_SMALL;
+    DevInfo dev;
+    if (int32_t e = current_device(&dev)) return e;
+
+    const bool vm = vocab_mode(M);
+    const int flags = (gumbel ? kFlagGumbel : 0) | (surface == SB_FULL_LOGITS ? kFlagFull : 0) |
+                      (out->target_ids ? kFlagTargets : 0);
+    const float inv_t = gumbel ? 1.0f / temperature : 1.0f;
+    GemmParams p{};
+    p.M = static_cast<int>(M);
+    p.d = static_cast<int>(d);
+    p.V = static_cast<int>(V);
+    p.k = k;
+    p.S = static_cast<int>(V / k);
+    p.T = T;
+    p.tv = vm ? kVocabTileV : kRowsTileN;
+    p.nb = vm ? static_cast<int>((M + 15) / 16 * 16) : kRowsTileN;
+    p.m_tiles = vm ? 1 : static_cast<int>((M + kTileA - 1) / kTileA);
+    const int64_t tiles = static_cast<int64_t>(k) * T * p.m_tiles;
+    if (tiles >= (int64_t(1) << 31)) return SB_ERR_INVALID_ARG;
+    p.num_tiles = static_cast<int>(tiles);
+    p.kblocks = static_cast<int>((d + kBlockK - 1) / kBlockK);
+    p.stages = lmhead_max_stages(p.nb, vm, flags);
+    p.flags = flags;
+    p.inv_t = inv_t;
+    p.seed = seed;
+    p.targets = out->target_ids;
+    p.logits = out->logits_bf16;
+    p.ws = ws_views(out->workspace, L, gumbel);
+    p.epoch = g_epoch.fetch_add(1) + 1;
+    p.timeout_ns = g_timeout_ns.load();
+    p.debug_stall = g_debug_stall.load();
+
+    CUtensorMap tmA, tmB;
+    const bool ok = vm ? (make_map(&tmA, W, V, d, kTileA) && make_map(&tmB, H, M, d, p.nb))
+                       : (make_map(&tmA, H, M, d, kTileA) && make_map(&tmB, W, V, d, kRowsTileN));
+    if (!ok) return SB_ERR_CUDA;
+    const int grid = static_cast<int>(tiles < dev.sms ? tiles : dev.sms);
+    const size_t smem = lmhead_smem_bytes(p.nb, p.stages, vm, flags);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (launch_lmhead(vm, tmA, tmB, p, grid, smem, st) != cudaSuccess) return SB_ERR_CUDA;
+    if (!with_combine) return SB_OK;
+    const CombineParams c = combine_params(out, p.ws, M, k, T, flags, inv_t);
+    if (launch_combine(c, st) != cudaSuccess) return SB_ERR_CUDA;
+    return SB_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t sb_lmhead_project(const void *H, const void *W, int64_t M, int64_t d, int64_t V,
+                          int32_t k, int32_t surface, float temperature, uint64_t seed,
+                          const sb_outputs *out, void *stream) {
+    return enqueue(H, W, M, d, V, k, surface, temperature, seed, out, stream, true);
+}
+
+int32_t sb_lmhead_records(const void *H, const void *W, int64_t M, int64_t d, int64_t V,
+                          int32_t k, int32_t surface, float temperature, uint64_t seed,
+                          const sb_outputs *out, void *stream) {
+    return enqueue(H, W, M, d, V, k, surface, temperature, seed, out, stream, false);
+}
+
+int32_t sb_combine_shard_records(const void *workspace, int64_t M, int32_t k,
+                                 int32_t tiles_per_shard_, int32_t surface, float temperature,
+                                 const sb_outputs *out, void *stream) {
+    if (!workspace || M < 1 || M > (int64_t(1) << 30) || k < 1 || tiles_per_shard_ < 1 ||
+        surface < SB_TOKEN || surface > SB_GUMBEL_TOKEN)
+        return SB_ERR_INVALID_ARG;
+    const bool gumbel = surface == SB_GUMBEL_TOKEN;
+    if (gumbel && !(std::isfinite(temperature) && temperature > 0.f)) return SB_ERR_INVALID_ARG;
+    if (int32_t e = check_outputs(out, surface == SB_FULL_LOGITS ? SB_TOKEN : surface, true))
+        return e;
+    if (out->workspace != workspace) return SB_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(M, k, tiles_per_shard_, gumbel);
+    if (out->workspace_bytes < L.total) return SB_ERR_WORKSPACE_TOO_SMALL;
+    DevInfo dev;
+    if (int32_t e = current_device(&dev)) return e;
+    const int flags = (gumbel ? kFlagGumbel : 0) | (out->target_ids ? kFlagTargets : 0);
+    const Workspace w = ws_views(const_cast<void *>(workspace), L, gumbel);
+    const CombineParams c = combine_params(out, w, M, k, tiles_per_shard_, flags,
+                                           gumbel ? 1.0f / temperature : 1.0f);
+    if (launch_combine(c, static_cast<cudaStream_t>(stream)) != cudaSuccess) return SB_ERR_CUDA;
+    return SB_OK;
+}
+
+int32_t sb_last_device_status(const sb_outputs *out) {
+    if (!out || !out->workspace || out->workspace_bytes < 16) return SB_ERR_INVALID_ARG;
+    uint64_t hdr[2] = {0, 0};
+    if (cudaMemcpy(hdr, out->workspace, sizeof hdr, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SB_ERR_CUDA;
+    const uint32_t epoch = static_cast<uint32_t>(hdr[0] & 0xFFFFFFFFu);
+    const uint64_t st = hdr[1];
+    if (static_cast<uint32_t>(st >> 32) == epoch && static_cast<uint32_t>(st) == SB_ERR_DEVICE_TIMEOUT)
+        return SB_ERR_DEVICE_TIMEOUT;
+    return SB_OK;
+}
+
+const char *sb_status_string(int32_t status) {
+    switch (status) {
+    case SB_OK: return "ok";
+    case SB_ERR_INVALID_ARG: return "invalid argument";
+    case SB_ERR_UNSUPPORTED: return "unsupported device (needs sm_103)";
+    case SB_ERR_ALIGNMENT: return "misaligned pointer or d not a multiple of 8";
+    case SB_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case SB_ERR_CUDA: return "CUDA runtime or driver error";
+    case SB_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+    }
+}
+
+int32_t sb_device_info(int32_t *num_sms, int32_t *cc) {
+    DevInfo dev;
+    const int32_t e = current_device(&dev);
+    if (e == SB_ERR_CUDA) return -1;
+    if (num_sms) *num_sms = dev.sms;
+    if (cc) *cc = dev.cc;
+    return 0;
+}
+
+int32_t sb_debug_configure(int32_t stall_epilogue, uint64_t wait_limit_ns) {
+    if (wait_limit_ns == 0) return SB_ERR_INVALID_ARG;
+    g_debug_stall.store(stall_epilogue ? 1 : 0);
+    g_timeout_ns.store(wait_limit_ns);
+    return SB_OK;
+}
+
+}  // extern "C"

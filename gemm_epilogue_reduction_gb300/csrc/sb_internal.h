@@ -1,0 +1,72 @@
+// sb_internal.h -- types shared by the libsb host code and its kernels (not part of the ABI).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace sb {
+
+constexpr int kBlockK = 64;          // K elements per pipeline stage (one 128-byte swizzle row)
+constexpr int kTileA = 128;          // rows of the MMA A operand (the UMMA M)
+constexpr int kRowsTileN = 256;      // vocabulary columns per tile when H rows are the A operand
+constexpr int kVocabTileV = 128;     // vocabulary columns per tile when W rows are the A operand
+constexpr int kMaxVocabModeRows = 256;  // largest M handled with W as the A operand
+constexpr int kMaxStages = 16;
+constexpr int kThreads = 192;        // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2-5 epilogue
+constexpr size_t kSmemLimit = 232448;  // 227 KB dynamic shared memory per CTA
+
+// Surface flags the kernels specialise on.
+enum : int { kFlagGumbel = 1, kFlagFull = 2, kFlagTargets = 4 };
+
+struct Workspace {       // device views into the caller's workspace
+    uint32_t *epoch;     // header word 0
+    unsigned long long *status;  // header word 1: (epoch << 32) | code
+    float *m;
+    int32_t *idx;
+    float *s;
+    float *gk;
+    int32_t *gi;
+    float *gz;
+    float *tz;
+};
+
+struct GemmParams {
+    int M, d, V, k, S, T;  // T = tiles per shard
+    int tv;                // vocabulary columns per tile
+    int nb;                // rows of the B operand per tile (UMMA N)
+    int m_tiles;           // tiles along M (1 when W rows are the A operand)
+    int num_tiles;
+    int kblocks;
+    int stages;
+    int flags;
+    float inv_t;
+    unsigned long long seed;
+    const int32_t *targets;
+    uint16_t *logits;
+    Workspace ws;
+    uint32_t epoch;
+    unsigned long long timeout_ns;
+    int debug_stall;
+};
+
+struct CombineParams {
+    int M, k, T;
+    int flags;
+    float inv_t;
+    Workspace ws;
+    int32_t *token;
+    float *token_logprob;
+    float *lse;
+    float *target_logprob;
+};
+
+// Launchers (lmhead.cu, combine.cu).  Return cudaSuccess or the launch error.
+cudaError_t launch_lmhead(bool vocab_mode, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                          const GemmParams &p, int grid, size_t smem, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
+
+size_t lmhead_smem_bytes(int nb, int stages, bool vocab_mode, int flags);
+int lmhead_max_stages(int nb, bool vocab_mode, int flags);
+
+}  // namespace sb

@@ -1,0 +1,195 @@
+/*
+ * sb.h -- C ABI of libsb: the LM-head contraction logits = H·Wᵀ over a vocabulary split
+ * into k contiguous lane shards, fused on one GPU (sm_103a) with the consumer-surface
+ * projection, so that only the surface the consumer asked for leaves the kernel.
+ *
+ * Source of the operation -- "SemBridge: Compiling Consumer Observations into
+ * Cross-Stack Communication Plans" (Chen, Zhu, Lin):
+ *   - Section 5.2 (Data, Result, and Control Paths): the tail output head materialises
+ *     full logits; a complete-logits or log-probability request slices them by TP lane
+ *     and rebuilds the full value; a token-only request applies the deterministic
+ *     sampler to the same tensor and sends int32 IDs.
+ *   - Section 2.2 (Consumer Surfaces and Delivery Obligations): the consumer surfaces are
+ *     complete logits, log-probabilities, token IDs or another registered projection.
+ *   - Section 3.1 (Boundary Contract): the registered projection operator names its
+ *     input/output types and deterministic tie-breaking (here: the lowest global
+ *     vocabulary index wins a tie).
+ *   - Figure 1: full-logit transfer and source projection expose the same token; they
+ *     differ only in where argmax runs.  Here argmax runs inside the GEMM epilogue.
+ *   - Section 5.2 also notes the transport reserves no persistent device-buffer pool;
+ *     likewise this library allocates no device memory: the caller owns every buffer.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named "device" must point to device memory of the current CUDA device
+ *     and be 16-byte aligned; sizes are element counts unless named *_bytes.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     All device work is enqueued asynchronously on it; nothing synchronises.
+ *   - The return value is an sb_status.  It covers argument validation and launch
+ *     errors only; when it is not SB_OK nothing was enqueued.  Errors found on the
+ *     device (a bounded wait that ran out) are recorded in the workspace status word
+ *     and read with sb_last_device_status() after the caller synchronises.
+ *   - There is no CPU fallback: a device that is not sm_103 returns SB_ERR_UNSUPPORTED.
+ *   - Calls that share a workspace must not overlap on the GPU (they would race on it).
+ */
+#ifndef SB_H
+#define SB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Consumer surface (Section 2.2).  Every surface produces the token; the surface
+ * decides which other outputs are mandatory and whether logits are written. */
+typedef enum sb_surface {
+    SB_TOKEN = 0,        /* deterministic argmax token (int32, lowest index on ties)      */
+    SB_TOKEN_LOGPROB = 1,/* token + its natural-log log-probability over the full vocab   */
+    SB_FULL_LOGITS = 2,  /* token + bf16 logits [M, V] in shard-to-full (global) layout    */
+    SB_GUMBEL_TOKEN = 3  /* counter-based Gumbel-max sample from softmax(z / T) + log-prob */
+} sb_surface;
+
+typedef enum sb_status {
+    SB_OK = 0,
+    SB_ERR_INVALID_ARG = 1,          /* a size, enum, pointer or temperature is out of range */
+    SB_ERR_UNSUPPORTED = 2,          /* the current device is not an sm_103 GPU               */
+    SB_ERR_ALIGNMENT = 3,            /* a pointer is not 16-byte aligned, or d % 8 != 0       */
+    SB_ERR_WORKSPACE_TOO_SMALL = 4,  /* workspace_bytes < sb_workspace_bytes(...)             */
+    SB_ERR_CUDA = 5,                 /* a CUDA runtime or driver call failed                  */
+    SB_ERR_DEVICE_TIMEOUT = 6        /* device side: a bounded wait gave up (after sync)      */
+} sb_status;
+
+/*
+ * Output buffers of one projection call.  All pointers are device pointers owned by the
+ * caller; NULL means "not requested".  Every surface fills every non-NULL output.
+ *   token           int32 [M]      required for every surface.
+ *   token_logprob   float [M]      log p(token); required for SB_TOKEN_LOGPROB and
+ *                                  SB_GUMBEL_TOKEN.  For SB_GUMBEL_TOKEN the distribution
+ *                                  is softmax(z / T), the one sampled from.
+ *   lse             float [M]      natural-log logsumexp of z (of z / T for SB_GUMBEL_TOKEN).
+ *   logits_bf16     uint16 [M*V]   bf16 bit patterns of z, row-major [M][V], column = the
+ *                                  global vocabulary index (lane shard s holds columns
+ *                                  [s*V/k, (s+1)*V/k)); required iff SB_FULL_LOGITS and
+ *                                  written only then.
+ *   target_ids      int32 [M]      optional scoring targets, each in [0, V).  Values out of
+ *                                  range are not detected and give an undefined result.
+ *   target_logprob  float [M]      log p(target_ids[r]); required iff target_ids != NULL.
+ *   workspace       bytes          scratch of at least sb_workspace_bytes(M, V, k, surface)
+ *                                  bytes, 256-byte aligned; holds the per-tile records, the
+ *                                  target logits and the device status word.  Its contents
+ *                                  need no initialisation.
+ */
+typedef struct sb_outputs {
+    int32_t *token;
+    float *token_logprob;
+    float *lse;
+    uint16_t *logits_bf16;
+    const int32_t *target_ids;
+    float *target_logprob;
+    void *workspace;
+    size_t workspace_bytes;
+} sb_outputs;
+
+/*
+ * Workspace layout (byte offsets from `workspace`; n = M * k * T with T =
+ * sb_tiles_per_shard(M, V, k); each array starts on a 256-byte boundary, in this order):
+ *   [0, 256)      header: uint32 epoch of the last launch, uint32 reserved,
+ *                 uint64 status word = (epoch << 32) | sb_status of that launch
+ *   float   m[n]     per-tile record: max of y over the tile's columns
+ *   int32   idx[n]   lowest global column attaining m
+ *   float   s[n]     sum over the tile of exp(y - m)
+ *   float   gkey[n]  SB_GUMBEL_TOKEN only: max of y + g over the tile
+ *   int32   gidx[n]  SB_GUMBEL_TOKEN only: lowest column attaining gkey
+ *   float   gz[n]    SB_GUMBEL_TOKEN only: z at gidx
+ *   float   tz[M]    z at target_ids[r] (written only when targets are given)
+ * Record (r, s, t) sits at index (r * k + s) * T + t and covers the global columns
+ * [s*S + t*TV, min(s*S + (t+1)*TV, (s+1)*S)) with S = V/k and the tile width TV = 128
+ * when M <= 256, else 256 (T = ceil(S / TV)).  y is z, or z * (1/T) for SB_GUMBEL_TOKEN
+ * with 1/T rounded to fp32 on the host; g is the Gumbel noise of sb_lmhead_project.
+ */
+
+/* Bytes of workspace one call needs; 0 if the arguments are invalid. */
+size_t sb_workspace_bytes(int64_t M, int64_t V, int32_t k, int32_t surface);
+
+/* Vocabulary tiles per lane shard T used for M rows (the record count per (row, shard));
+ * -1 if the arguments are invalid. */
+int32_t sb_tiles_per_shard(int64_t M, int64_t V, int32_t k);
+
+/*
+ * One projection call: logits z = H·Wᵀ (fp32 accumulation on the tensor cores, no bias,
+ * scale or soft-cap), projected per Section 5.2 onto `surface`, in two kernels enqueued on
+ * `stream` -- the fused GEMM + record epilogue, then the record combine
+ * (sb_combine_shard_records) -- with no host synchronisation.
+ *   H          device bf16 [M, d] row-major (K-major), 16-byte aligned.
+ *   W          device bf16 [V, d] row-major (the output-head weight), 16-byte aligned.
+ *   M, d, V    M >= 1, d >= 8 with d % 8 == 0, V >= 1.
+ *   k          number of contiguous lane shards, k >= 1 and V % k == 0.
+ *   surface    an sb_surface.
+ *   temperature  SB_GUMBEL_TOKEN: finite and > 0 (the key is z * (1/T) + g); ignored
+ *              otherwise.
+ *   seed       SB_GUMBEL_TOKEN: the SplitMix64 stream seed.  Column j of row r draws the
+ *              output at stream index n = r*V + j, i.e. the SplitMix64 finaliser of
+ *              seed + (n + 1) * 0x9E3779B97F4A7C15; u = (x >> 40) * 2^-24 and
+ *              g = -log(-log u) in fp32 (u = 0 gives g = -inf).  Ignored otherwise.
+ *   out        outputs and workspace (see sb_outputs); read on the host during the call.
+ * Returns SB_OK, or an error with nothing enqueued.
+ */
+int32_t sb_lmhead_project(const void *H, const void *W, int64_t M, int64_t d, int64_t V,
+                          int32_t k, int32_t surface, float temperature, uint64_t seed,
+                          const sb_outputs *out, void *stream);
+
+/*
+ * The first kernel of sb_lmhead_project alone: the fused GEMM + record epilogue, which
+ * writes the per-tile records (and the target logits) into out->workspace and, for
+ * SB_FULL_LOGITS, the bf16 logits; token, log-prob and lse outputs are left unwritten.
+ * Same arguments, validation and return values as sb_lmhead_project.  It is the step a
+ * vocabulary-sharded caller runs before exchanging records (Section 5.2: each TP lane
+ * projects its own shard) and then finishing with sb_combine_shard_records.
+ */
+int32_t sb_lmhead_records(const void *H, const void *W, int64_t M, int64_t d, int64_t V,
+                          int32_t k, int32_t surface, float temperature, uint64_t seed,
+                          const sb_outputs *out, void *stream);
+
+/*
+ * The record combine alone (the second kernel of sb_lmhead_project): reads the per-tile
+ * records of `workspace` (layout above; tiles_per_shard = T) and writes token,
+ * token_logprob, lse and target_logprob of `out` (those that are non-NULL).  Per row it
+ * merges the T records of each shard in a fixed tree (shard-local completion), then the k
+ * shard results in ascending shard order (the cross-shard merge that replaces "AllGather
+ * the logits, then argmax" of Section 5.2).  The merge of two records keeps the larger
+ * max, the lower index on an equal max, and rescales the exp-sums to the new max; the
+ * fixed order makes the output bits a function of the record bits alone.
+ *   temperature  as for sb_lmhead_project (used by SB_GUMBEL_TOKEN and the target
+ *              log-prob only).
+ *   out->logits_bf16 is ignored; out->workspace must equal `workspace`.
+ */
+int32_t sb_combine_shard_records(const void *workspace, int64_t M, int32_t k,
+                                 int32_t tiles_per_shard, int32_t surface, float temperature,
+                                 const sb_outputs *out, void *stream);
+
+/* Device status of the last call that used out->workspace: SB_OK or
+ * SB_ERR_DEVICE_TIMEOUT.  Synchronous: copies the header to the host (call it after
+ * synchronising the stream).  Returns SB_ERR_CUDA if the copy fails. */
+int32_t sb_last_device_status(const sb_outputs *out);
+
+/* Static description of a status code; never NULL. */
+const char *sb_status_string(int32_t status);
+
+/* Number of SMs and compute capability (major * 10 + minor) of the current device, as the
+ * library sees them; -1 without a usable device. */
+int32_t sb_device_info(int32_t *num_sms, int32_t *cc);
+
+/* Test hook for the device watchdog.  stall_epilogue != 0 makes the epilogue warps of
+ * later sb_lmhead_project calls wait on a barrier that nothing ever arrives at, so their
+ * bounded wait runs out and the call reports SB_ERR_DEVICE_TIMEOUT through
+ * sb_last_device_status (the outputs are then undefined).  wait_limit_ns (> 0) is the
+ * time limit of every device-side wait (default 2 s).  Process-wide; not for production.
+ * Returns SB_ERR_INVALID_ARG for wait_limit_ns == 0. */
+int32_t sb_debug_configure(int32_t stall_epilogue, uint64_t wait_limit_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SB_H */

@@ -1,0 +1,111 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and loads, exports
+every entry point the header declares, sizes its workspace as documented, and rejects bad
+arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gemm_epilogue_reduction_gb300 as sb
+from gemm_epilogue_reduction_gb300 import build as sbbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sb.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    sbbuild.build()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(sb_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ["sb_workspace_bytes", "sb_tiles_per_shard", "sb_lmhead_project",
+              "sb_combine_shard_records", "sb_last_device_status", "sb_status_string"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(sbbuild.LIB_PATH)
+    for n in _declared():
+        assert hasattr(lib, n), n
+
+
+def test_tiles_per_shard_and_workspace_layout():
+    # decode: W rows are the MMA A operand, 128-column vocabulary tiles
+    assert sb.sb_tiles_per_shard(16, 151936, 4) == (37984 + 127) // 128 == 297
+    # prefill: 256-column tiles
+    assert sb.sb_tiles_per_shard(4096, 200064, 4) == (50016 + 255) // 256 == 196
+    assert sb.sb_tiles_per_shard(256, 151936, 4) == 297
+    assert sb.sb_tiles_per_shard(257, 151936, 4) == 149
+    assert sb.sb_tiles_per_shard(4, 4097, 2) == -1  # V % k != 0
+
+    def al(x):
+        return (x + 255) // 256 * 256
+
+    M, V, k = 16, 151936, 4
+    n = M * k * 297
+    assert sb.sb_workspace_bytes(M, V, k, sb.SB_TOKEN) == 256 + 3 * al(4 * n) + al(4 * M)
+    assert sb.sb_workspace_bytes(M, V, k, sb.SB_GUMBEL_TOKEN) == 256 + 6 * al(4 * n) + al(4 * M)
+    assert sb.sb_workspace_bytes(0, V, k, sb.SB_TOKEN) == 0
+    assert sb.sb_workspace_bytes(M, V, k, 7) == 0
+
+
+def test_status_strings():
+    for code in range(7):
+        assert sb.sb_status_string(code)
+    assert sb.sb_status_string(99) == "unknown status"
+
+
+def _outputs(ws_bytes=1 << 20, **kw):
+    base = 0x10000000
+    fields = dict(token=base, token_logprob=base + 0x1000, lse=base + 0x2000, logits_bf16=None,
+                  target_ids=None, target_logprob=None, workspace=base + 0x100000,
+                  workspace_bytes=ws_bytes)
+    fields.update(kw)
+    return sb.sb_outputs(**fields)
+
+
+@pytest.mark.parametrize("case, expect", [
+    (dict(H=None), sb.SB_ERR_INVALID_ARG),
+    (dict(M=0), sb.SB_ERR_INVALID_ARG),
+    (dict(V=4097), sb.SB_ERR_INVALID_ARG),      # V % k != 0
+    (dict(k=0), sb.SB_ERR_INVALID_ARG),
+    (dict(surface=4), sb.SB_ERR_INVALID_ARG),
+    (dict(d=4), sb.SB_ERR_INVALID_ARG),
+    (dict(d=260), sb.SB_ERR_ALIGNMENT),          # d % 8 != 0
+    (dict(H=0x10000008), sb.SB_ERR_ALIGNMENT),
+    (dict(surface=sb.SB_GUMBEL_TOKEN, T=0.0), sb.SB_ERR_INVALID_ARG),
+    (dict(surface=sb.SB_GUMBEL_TOKEN, T=float("inf")), sb.SB_ERR_INVALID_ARG),
+    (dict(surface=sb.SB_FULL_LOGITS), sb.SB_ERR_INVALID_ARG),  # logits buffer missing
+    (dict(out=dict(token=None)), sb.SB_ERR_INVALID_ARG),
+    (dict(out=dict(token_logprob=None), surface=sb.SB_TOKEN_LOGPROB), sb.SB_ERR_INVALID_ARG),
+    (dict(out=dict(target_ids=0x20000000)), sb.SB_ERR_INVALID_ARG),  # no target_logprob
+    (dict(out=dict(workspace=0x10000010)), sb.SB_ERR_ALIGNMENT),
+    (dict(out=dict(workspace_bytes=1024)), sb.SB_ERR_WORKSPACE_TOO_SMALL),
+])
+def test_invalid_arguments_are_rejected_before_any_launch(case, expect):
+    args = dict(H=0x30000000, W=0x40000000, M=4, d=256, V=4096, k=2, surface=sb.SB_TOKEN,
+                T=1.0)
+    args.update({k: v for k, v in case.items() if k != "out"})
+    out = _outputs(**case.get("out", {}))
+    st = sb.sb_lmhead_project(args["H"], args["W"], args["M"], args["d"], args["V"],
+                              args["k"], args["surface"], args["T"], 0, out, 0)
+    assert st == expect
+
+
+def test_valid_arguments_without_a_gpu_report_a_device_error():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("this machine has a GPU")
+    out = _outputs()
+    st = sb.sb_lmhead_project(0x30000000, 0x40000000, 4, 256, 4096, 2, sb.SB_TOKEN, 1.0, 0,
+                              out, 0)
+    assert st in (sb.SB_ERR_CUDA, sb.SB_ERR_UNSUPPORTED)

@@ -1,0 +1,154 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle, element by element,
+on seeded inputs that span several tiles and ragged tails in every dimension."""
+import numpy as np
+import pytest
+import torch
+
+import gemm_epilogue_reduction_gb300 as sb
+import oracle
+from gemm_epilogue_reduction_gb300 import synth
+from gpu_helpers import TOL, bf16_half_ulp, check_rows, run_and_check
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def test_tiny_workload_token_and_logprob():
+    """M=4, d=256, V=4096, k=2 (S=2048), seed 0; TOKEN and TOKEN_LOGPROB."""
+    for surface in (sb.SB_TOKEN, sb.SB_TOKEN_LOGPROB):
+        run_and_check(4, 256, 4096, 2, surface, targets=True)
+
+
+# (M, d, V, k): vocab mode for M <= 256 (128-column tiles), rows mode above (256-column
+# tiles); tails in M (not a multiple of 16 / 128), d (not a multiple of 64), S (not a
+# multiple of the tile width), single shard, V == k, d == 8.
+SHAPES = [
+    (1, 64, 1000, 1),
+    (3, 72, 3000, 3),
+    (16, 256, 4096, 4),
+    (17, 128, 2560, 5),
+    (40, 8, 300, 3),
+    (64, 512, 6000, 2),
+    (100, 200, 1000, 4),
+    (5, 256, 7, 7),
+    (256, 128, 2048, 2),
+    (257, 128, 2048, 2),
+    (300, 136, 3000, 3),
+    (513, 64, 1024, 1),
+]
+
+
+@pytest.mark.parametrize("M,d,V,k", SHAPES)
+def test_shapes_token_logprob_targets(M, d, V, k):
+    run_and_check(M, d, V, k, sb.SB_TOKEN_LOGPROB, seed=M + d, targets=True)
+
+
+@pytest.mark.parametrize("M,d,V,k", [(4, 256, 4096, 2), (64, 128, 3000, 2), (300, 64, 1000, 2),
+                                     (7, 64, 333, 3)])
+def test_full_logits_values_and_tokens(M, d, V, k):
+    """FULL_LOGITS writes z in bf16 at its global column; its token equals TOKEN's."""
+    res, ref, HW = run_and_check(M, d, V, k, sb.SB_FULL_LOGITS, seed=11, targets=True)
+    tok = sb.project(*HW, k, sb.SB_TOKEN)
+    torch.cuda.synchronize()
+    assert torch.equal(tok["token"], res["token"])
+    # argmax of the written logits in fp32 agrees with the token wherever the bf16 rounding
+    # cannot reorder the top two (the R0 and P0 token surfaces of Figure 1)
+    lg = res["logits"].float()
+    am = lg.argmax(dim=1).cpu().numpy()
+    gap = ref["key_top1"] - ref["key_top2"]
+    safe = gap > 2 * (TOL + bf16_half_ulp(ref["key_top1"]))
+    assert np.array_equal(am[safe], res["token"].cpu().numpy()[safe])
+
+
+@pytest.mark.parametrize("M,d,V,k", [(64, 128, 3000, 3), (300, 64, 2000, 2), (3, 64, 512, 1)])
+def test_gumbel_sampling_parity(M, d, V, k):
+    run_and_check(M, d, V, k, sb.SB_GUMBEL_TOKEN, seed=5, T=0.7, gseed=1234, targets=True)
+
+
+@pytest.mark.parametrize("M", [8, 300])
+def test_exact_ties_pick_the_lowest_global_index(M):
+    """Duplicated W rows give bit-identical logits in different tiles and shards; the
+    token is the lowest such column in every merge."""
+    d, V, k = 64, 2048, 4
+    H, W = synth.make_hw(M, d, V, seed=3)
+    big = (H[0].float() * 6.0 / d).to(torch.bfloat16)
+    W = W.clone()
+    W[1500] = big
+    W = synth.duplicate_rows(W, [(1500, 700), (1500, 701), (1500, 1999)])
+    res = sb.project(H.cuda(), W.cuda(), k, sb.SB_TOKEN)
+    torch.cuda.synchronize()
+    ref = oracle.project(synth.bf16_bits(H)[:1], synth.bf16_bits(W), k)
+    assert ref["token"][0] == 700
+    assert int(res["token"][0]) == 700
+
+
+def test_k_invariance_of_logits_and_tokens():
+    """The K-reduction of each logit does not depend on the lane split, so the bf16 logits
+    are bitwise identical for k = 1, 2, 4 and so are the tokens."""
+    M, d, V = 32, 256, 4096
+    H, W = synth.make_hw(M, d, V, seed=9)
+    H, W = H.cuda(), W.cuda()
+    outs = [sb.project(H, W, k, sb.SB_FULL_LOGITS) for k in (1, 2, 4)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o["logits"], outs[0]["logits"])
+        assert torch.equal(o["token"], outs[0]["token"])
+
+
+def test_combine_is_deterministic_bitwise():
+    """Identical records give identical output bits: two full calls, and the combine
+    re-run alone on the same workspace."""
+    M, d, V, k = 48, 128, 5000, 5
+    H, W = synth.make_hw(M, d, V, seed=21)
+    H, W = H.cuda(), W.cuda()
+    tg = synth.make_targets(M, V, device="cuda")
+    a = sb.project(H, W, k, sb.SB_TOKEN_LOGPROB, targets=tg)
+    b = sb.project(H, W, k, sb.SB_TOKEN_LOGPROB, targets=tg)
+    torch.cuda.synchronize()
+    for key in ("token", "token_logprob", "lse", "target_logprob"):
+        assert torch.equal(a[key], b[key]), key
+    c_out, c = sb.make_outputs(M, V, k, sb.SB_TOKEN_LOGPROB, targets=tg, workspace=a["workspace"])
+    T = sb.sb_tiles_per_shard(M, V, k)
+    st = sb.sb_combine_shard_records(a["workspace"], M, k, T, sb.SB_TOKEN_LOGPROB, 1.0, c_out)
+    assert st == sb.SB_OK
+    torch.cuda.synchronize()
+    for key in ("token", "token_logprob", "lse", "target_logprob"):
+        assert torch.equal(a[key], c[key]), key
+
+
+def test_token_surface_leaves_a_logits_buffer_untouched():
+    """The token surfaces never write logits: a sentinel-filled buffer passed alongside
+    stays as it was."""
+    M, d, V, k = 16, 128, 4096, 2
+    H, W = synth.make_hw(M, d, V, seed=1)
+    H, W = H.cuda(), W.cuda()
+    out, bufs = sb.make_outputs(M, V, k, sb.SB_TOKEN_LOGPROB)
+    sentinel = torch.full((M, V), 12345, dtype=torch.int16, device="cuda")
+    out.logits_bf16 = sentinel.data_ptr()
+    assert sb.sb_lmhead_project(H, W, M, d, V, k, sb.SB_TOKEN_LOGPROB, 1.0, 0, out) == sb.SB_OK
+    torch.cuda.synchronize()
+    assert bool((sentinel == 12345).all())
+
+
+def test_device_watchdog_reports_timeout_and_context_survives():
+    """A wait that nothing will satisfy runs out after the configured limit; the kernel
+    records SB_ERR_DEVICE_TIMEOUT, releases TMEM and exits; the next call is correct."""
+    M, d, V, k = 16, 128, 2048, 2
+    H, W = synth.make_hw(M, d, V, seed=2)
+    H, W = H.cuda(), W.cuda()
+    try:
+        assert sb.sb_debug_configure(True, 20_000_000) == sb.SB_OK  # 20 ms
+        res = sb.project(H, W, k, sb.SB_TOKEN)
+        torch.cuda.synchronize()
+        assert sb.sb_last_device_status(res["_outputs"]) == sb.SB_ERR_DEVICE_TIMEOUT
+    finally:
+        sb.sb_debug_configure(False, 2_000_000_000)
+    run_and_check(M, d, V, k, sb.SB_TOKEN_LOGPROB, HW=(H, W))
+    res = sb.project(H, W, k, sb.SB_TOKEN)
+    torch.cuda.synchronize()
+    assert sb.sb_last_device_status(res["_outputs"]) == sb.SB_OK
