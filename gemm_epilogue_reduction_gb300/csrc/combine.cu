@@ -13,6 +13,7 @@
 //   per (row, shard): lane l of one warp folds tiles l, l+32, ... in ascending order, then
 //                     an xor butterfly (16, 8, 4, 2, 1) merges the 32 lane results;
 //   per row:          the k shard results merge in ascending shard order.
+// One block serves one row; its warps take the shards round-robin.
 // The output bits are therefore a function of the record bits alone (any grid, any run).
 #include <climits>
 
@@ -46,25 +47,53 @@ __device__ __forceinline__ GRec gmerge(const GRec &a, const GRec &b) {
     return (a.k > b.k || (a.k == b.k && a.i < b.i)) ? a : b;
 }
 
+constexpr int kMaxWarps = 8;
+constexpr int kBatch = 8;  // records each lane loads before folding them
+
+// One block per row; warp w completes shards w, w + 8, ... (lane l folds tiles l, l+32, ...
+// in ascending order, loading kBatch of them at a time, then the xor butterfly), writes the
+// shard record to shared memory, and thread 0 merges the k shard records in ascending order.
 template <bool GUMBEL>
-__global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
+__global__ void __launch_bounds__(32 * kMaxWarps) combine_kernel(const CombineParams p) {
+    extern __shared__ float sh[];  // k records: m, i, s [, gk, gi, gz]
+    float *sm = sh;
+    int *si = reinterpret_cast<int *>(sh + p.k);
+    float *ss = sh + 2 * p.k;
+    float *sgk = sh + 3 * p.k;
+    int *sgi = reinterpret_cast<int *>(sh + 4 * p.k);
+    float *sgz = sh + 5 * p.k;
     const int lane = threadIdx.x & 31;
-    const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (row >= p.M) return;
-    Rec acc{-INFINITY, INT_MAX, 0.f};
-    GRec gacc{-INFINITY, INT_MAX, 0.f};
-    for (int sh = 0; sh < p.k; ++sh) {
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int row = blockIdx.x;
+    // Launched as a programmatic dependent of the GEMM: wait until that grid has completed
+    // and its record writes are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int sh_i = warp; sh_i < p.k; sh_i += nwarps) {
         Rec r{-INFINITY, INT_MAX, 0.f};
         GRec g{-INFINITY, INT_MAX, 0.f};
-        const size_t base = (static_cast<size_t>(row) * p.k + sh) * p.T;
-        for (int t = lane; t < p.T; t += 32) {
-            const Rec x{__ldg(p.ws.m + base + t), __ldg(p.ws.idx + base + t),
-                        __ldg(p.ws.s + base + t)};
-            r = merge(r, x);
-            if (GUMBEL) {
-                const GRec y{__ldg(p.ws.gk + base + t), __ldg(p.ws.gi + base + t),
-                             __ldg(p.ws.gz + base + t)};
-                g = gmerge(g, y);
+        const size_t base = (static_cast<size_t>(row) * p.k + sh_i) * p.T;
+        for (int t0 = lane; t0 < p.T; t0 += 32 * kBatch) {
+            Rec x[kBatch];
+            GRec y[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int t = t0 + 32 * u;
+                if (t < p.T) {
+                    x[u] = Rec{__ldg(p.ws.m + base + t), __ldg(p.ws.idx + base + t),
+                               __ldg(p.ws.s + base + t)};
+                    if (GUMBEL)
+                        y[u] = GRec{__ldg(p.ws.gk + base + t), __ldg(p.ws.gi + base + t),
+                                    __ldg(p.ws.gz + base + t)};
+                } else {
+                    x[u] = Rec{-INFINITY, INT_MAX, 0.f};
+                    if (GUMBEL) y[u] = GRec{-INFINITY, INT_MAX, 0.f};
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                r = merge(r, x[u]);
+                if (GUMBEL) g = gmerge(g, y[u]);
             }
         }
 #pragma unroll
@@ -80,31 +109,51 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
                 g = gmerge(g, go);
             }
         }
-        acc = merge(acc, r);
-        if (GUMBEL) gacc = gmerge(gacc, g);
-    }
-    if (lane == 0) {
-        const float lse = acc.m + logf(acc.s);
-        p.token[row] = GUMBEL ? gacc.i : acc.i;
-        if (p.lse) p.lse[row] = lse;
-        if (p.token_logprob) p.token_logprob[row] = GUMBEL ? gacc.z * p.inv_t - lse : -logf(acc.s);
-        if (p.target_logprob) {
-            const float tz = p.ws.tz[row];
-            p.target_logprob[row] = (GUMBEL ? tz * p.inv_t : tz) - lse;
+        if (lane == 0) {
+            sm[sh_i] = r.m;
+            si[sh_i] = r.i;
+            ss[sh_i] = r.s;
+            if (GUMBEL) {
+                sgk[sh_i] = g.k;
+                sgi[sh_i] = g.i;
+                sgz[sh_i] = g.z;
+            }
         }
+    }
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    Rec acc{-INFINITY, INT_MAX, 0.f};
+    GRec gacc{-INFINITY, INT_MAX, 0.f};
+    for (int s2 = 0; s2 < p.k; ++s2) {
+        acc = merge(acc, Rec{sm[s2], si[s2], ss[s2]});
+        if (GUMBEL) gacc = gmerge(gacc, GRec{sgk[s2], sgi[s2], sgz[s2]});
+    }
+    const float lse = acc.m + logf(acc.s);
+    p.token[row] = GUMBEL ? gacc.i : acc.i;
+    if (p.lse) p.lse[row] = lse;
+    if (p.token_logprob) p.token_logprob[row] = GUMBEL ? gacc.z * p.inv_t - lse : -logf(acc.s);
+    if (p.target_logprob) {
+        const float tz = p.ws.tz[row];
+        p.target_logprob[row] = (GUMBEL ? tz * p.inv_t : tz) - lse;
     }
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
-    constexpr int kRowsPerBlock = 8;
-    const int grid = (p.M + kRowsPerBlock - 1) / kRowsPerBlock;
-    if (p.flags & kFlagGumbel)
-        combine_kernel<true><<<grid, 32 * kRowsPerBlock, 0, stream>>>(p);
-    else
-        combine_kernel<false><<<grid, 32 * kRowsPerBlock, 0, stream>>>(p);
-    return cudaGetLastError();
+    const int warps = p.k < kMaxWarps ? p.k : kMaxWarps;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(p.M);
+    cfg.blockDim = dim3(32 * warps);
+    cfg.dynamicSmemBytes = static_cast<size_t>(p.k) * ((p.flags & kFlagGumbel) ? 24 : 12);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (p.flags & kFlagGumbel) return cudaLaunchKernelEx(&cfg, combine_kernel<true>, p);
+    return cudaLaunchKernelEx(&cfg, combine_kernel<false>, p);
 }
 
 }  // namespace sb

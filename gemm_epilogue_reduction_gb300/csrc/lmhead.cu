@@ -438,6 +438,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Let the record combine (a programmatic dependent launch) get scheduled early; it
+    // waits for this whole grid to finish before it reads any record.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (one lane)

@@ -71,7 +71,7 @@ Workspace ws_views(void *base, const WsLayout &L, bool gumbel) {
 
 bool shape_ok(int64_t M, int64_t V, int32_t k) {
     return M >= 1 && M <= (int64_t(1) << 30) && V >= 1 && V < (int64_t(1) << 31) && k >= 1 &&
-           V % k == 0;
+           k <= kMaxShards && V % k == 0;
 }
 
 bool vocab_mode(int64_t M) { return M <= kMaxVocabModeRows; }
@@ -266,7 +266,8 @@ int32_t sb_lmhead_records(const void *H, const void *W, int64_t M, int64_t d, in
 int32_t sb_combine_shard_records(const void *workspace, int64_t M, int32_t k,
                                  int32_t tiles_per_shard_, int32_t surface, float temperature,
                                  const sb_outputs *out, void *stream) {
-    if (!workspace || M < 1 || M > (int64_t(1) << 30) || k < 1 || tiles_per_shard_ < 1 ||
+    if (!workspace || M < 1 || M > (int64_t(1) << 30) || k < 1 || k > kMaxShards ||
+        tiles_per_shard_ < 1 ||
         surface < SB_TOKEN || surface > SB_GUMBEL_TOKEN)
         return SB_ERR_INVALID_ARG;
     const bool gumbel = surface == SB_GUMBEL_TOKEN;

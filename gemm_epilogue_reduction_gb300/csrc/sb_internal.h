@@ -13,6 +13,7 @@ constexpr int kRowsTileN = 256;      // vocabulary columns per tile when H rows 
 constexpr int kVocabTileV = 128;     // vocabulary columns per tile when W rows are the A operand
 constexpr int kMaxVocabModeRows = 256;  // largest M handled with W as the A operand
 constexpr int kMaxStages = 16;
+constexpr int kMaxShards = 1024;     // largest k (the combine keeps k shard records in smem)
 constexpr int kThreads = 192;        // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2-5 epilogue
 constexpr size_t kSmemLimit = 232448;  // 227 KB dynamic shared memory per CTA
 

@@ -124,7 +124,7 @@ int32_t sb_tiles_per_shard(int64_t M, int64_t V, int32_t k);
  *   H          device bf16 [M, d] row-major (K-major), 16-byte aligned.
  *   W          device bf16 [V, d] row-major (the output-head weight), 16-byte aligned.
  *   M, d, V    M >= 1, d >= 8 with d % 8 == 0, V >= 1.
- *   k          number of contiguous lane shards, k >= 1 and V % k == 0.
+ *   k          number of contiguous lane shards, 1 <= k <= 1024 and V % k == 0.
  *   surface    an sb_surface.
  *   temperature  SB_GUMBEL_TOKEN: finite and > 0 (the key is z * (1/T) + g); ignored
  *              otherwise.
