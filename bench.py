@@ -48,6 +48,14 @@ WORKLOADS = {
                      desc="seeded sampling: H[256,5120] x W[151936,5120] bf16, k=4, GUMBEL_TOKEN T=0.7"),
     "tiny": dict(M=4, d=256, V=4096, k=2, surface="token_logprob",
                  desc="tiny: H[4,256] x W[4096,256] bf16, k=2"),
+    # smaller cases of the same kernels for ncu captures (inputs still larger than L2)
+    "decode16_small": dict(M=16, d=1024, V=151936, k=4, surface="token_logprob",
+                           desc="profiling case: H[16,1024] x W[151936,1024] bf16, k=4"),
+    "prefill_small": dict(M=1024, d=2048, V=65536, k=4, surface="token_logprob", targets=True,
+                          desc="profiling case: H[1024,2048] x W[65536,2048] bf16, k=4"),
+    "sampling_small": dict(M=256, d=1024, V=151936, k=4, surface="gumbel_token", T=0.7,
+                           seed=1234,
+                           desc="profiling case: H[256,1024] x W[151936,1024] bf16, k=4, GUMBEL"),
 }
 METRIC = "LM-head+projection rows/s; % of HBM GB/s (decode) or bf16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -322,7 +330,7 @@ def main():
     peaks, peak_src = load_peaks()
     alg_bytes = V * d * 2 + M * d * 2 + M * 12 + (M * V * 2 if surface == sb.SB_FULL_LOGITS else 0)
     alg_flops = 2.0 * M * V * d
-    mem_bound = args.workload in ("decode16", "decode64", "tiny", "sampling")
+    mem_bound = not args.workload.startswith("prefill")
     achieved_gbs = alg_bytes / (gemm_avg * 1e-3) / 1e9
     achieved_tfs = alg_flops / (gemm_avg * 1e-3) / 1e12
     tr = KERNEL_TRAFFIC.get(args.workload)
