@@ -65,6 +65,8 @@ def lib():
         L.sb_lmhead_project.restype = i32
         L.sb_lmhead_records.argtypes = L.sb_lmhead_project.argtypes
         L.sb_lmhead_records.restype = i32
+        L.sb_lmhead_project_static_scratch.argtypes = L.sb_lmhead_project.argtypes
+        L.sb_lmhead_project_static_scratch.restype = i32
         L.sb_combine_shard_records.argtypes = [P, i64, i32, i32, i32, ctypes.c_float,
                                                ctypes.POINTER(sb_outputs), P]
         L.sb_combine_shard_records.restype = i32
@@ -118,6 +120,15 @@ def sb_lmhead_records(H, W, M, d, V, k, surface, temperature, seed, out: sb_outp
     return int(lib().sb_lmhead_records(_ptr(H), _ptr(W), M, d, V, k, surface,
                                        float(temperature), seed & (2**64 - 1),
                                        ctypes.byref(out), _stream(stream)))
+
+
+def sb_lmhead_project_static_scratch(H, W, M, d, V, k, surface, temperature, seed,
+                                     out: sb_outputs, stream=None) -> int:
+    """sb_lmhead_project with the library's built-in 8 MiB scratch instead of
+    out.workspace, for callers that cannot allocate device memory."""
+    return int(lib().sb_lmhead_project_static_scratch(_ptr(H), _ptr(W), M, d, V, k, surface,
+                                                      float(temperature), seed & (2**64 - 1),
+                                                      ctypes.byref(out), _stream(stream)))
 
 
 def sb_combine_shard_records(workspace, M, k, tiles_per_shard, surface, temperature,

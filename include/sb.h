@@ -168,6 +168,31 @@ int32_t sb_combine_shard_records(const void *workspace, int64_t M, int32_t k,
                                  int32_t tiles_per_shard, int32_t surface, float temperature,
                                  const sb_outputs *out, void *stream);
 
+/*
+ * sb_lmhead_project without a caller-supplied workspace (the SemBridge paper has no
+ * counterpart; this entry point exists for callers that cannot allocate device memory).
+ * Some callers cannot call cudaMalloc: a plug-in inside a host engine that owns the whole
+ * device-memory pool, code on a latency-critical path where cudaMalloc's implicit device
+ * synchronisation is not allowed, or a foreign-function caller that links only this
+ * library.  This call takes its scratch from an 8 MiB array compiled into the library
+ * (every GPU that loads libsb holds it until the process exits) and allocates nothing.
+ *   Arguments, outputs and return values are those of sb_lmhead_project, except that
+ *   out->workspace and out->workspace_bytes are ignored.  A problem whose
+ *   sb_workspace_bytes(M, V, k, surface) exceeds 8 MiB (8388608 bytes) is rejected with
+ *   SB_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *   The first call on each device looks up the array's device address (with that device
+ *   current); make that first call before any stream capture.
+ *   Every call on a device shares the one array and leaves its records there; nothing in
+ *   it needs clearing between calls, but calls that overlap on the GPU (different streams,
+ *   or host threads without ordering) race on it and give undefined results.
+ *   The device status word also lives in the array, so a device-side timeout of this call
+ *   is not reported (sb_last_device_status cannot reach it).
+ */
+int32_t sb_lmhead_project_static_scratch(const void *H, const void *W, int64_t M, int64_t d,
+                                         int64_t V, int32_t k, int32_t surface,
+                                         float temperature, uint64_t seed,
+                                         const sb_outputs *out, void *stream);
+
 /* Device status of the last call that used out->workspace: SB_OK or
  * SB_ERR_DEVICE_TIMEOUT.  Synchronous: copies the header to the host (call it after
  * synchronising the stream).  Returns SB_ERR_CUDA if the copy fails. */
