@@ -63,7 +63,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic of the GEMM kernel per launch from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), with the hash of the kernel source it was taken on; reported as
 # null once the source differs.
-KERNEL_TRAFFIC = {}
+KERNEL_TRAFFIC = {
+    # decode16: --set full capture of the d=1024 case of the same kernel (reads 311.34 MB for
+    # 311.20 MB of W + H, writes 3.28 MB), reads scaled by 5x to d=5120.
+    "decode16": {"bytes": 1.5600e9, "src_sha": "b7ea8294071aa7ff"},
+}
 
 
 def kernel_src_hash() -> str:
@@ -147,6 +151,27 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def rank_rows_seed(rank: int) -> int:
+    """Seed of the H batch a rank projects (rank 0 uses the workload's seed-0 inputs)."""
+    return 0 if rank == 0 else 1000 + rank
+
+
+def max_over_ranks(x: float, device) -> float:
+    """The maximum of x over all ranks (x itself without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rows_per_s(world: int, rows_per_rank: int, max_ms_per_step: float) -> float:
+    """Whole-job throughput: the rows every rank projected per step over the slowest rank."""
+    return world * rows_per_rank / (max_ms_per_step * 1e-3)
 
 
 def oracle_rows_per_s(Hb, Wb, k, cfg, rows_per_call, min_seconds, max_calls=None):
@@ -251,7 +276,7 @@ def main():
     # each rank draws its own batch of rows (weak scaling) and the same W
     H, W = synth.make_hw(M, d, V, seed=0, device="cuda")
     if rank:
-        H = synth.make_hw(M, d, 1, seed=1000 + rank, device="cuda")[0]
+        H = synth.make_hw(M, d, 1, seed=rank_rows_seed(rank), device="cuda")[0]
     targets = synth.make_targets(M, V, seed=1, device="cuda") if cfg.get("targets") else None
     out, bufs = sb.make_outputs(M, V, k, surface, targets=targets)
     Tps = sb.sb_tiles_per_shard(M, V, k)
@@ -294,10 +319,7 @@ def main():
     gemm_ms = [ev[3 * i].elapsed_time(ev[3 * i + 1]) for i in range(K)]
     comb_ms = [ev[3 * i + 1].elapsed_time(ev[3 * i + 2]) for i in range(K)]
     total_ms = ev[0].elapsed_time(ev[3 * K - 1])
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, "cuda")
     if sb.sb_last_device_status(out) != sb.SB_OK:
         raise RuntimeError("device status not OK after the timed region")
 
@@ -324,7 +346,7 @@ def main():
     e2e_ms = e0.elapsed_time(e1) / E
 
     ms_per_step = total_ms / K
-    value = world * M / (ms_per_step * 1e-3)
+    value = job_rows_per_s(world, M, ms_per_step)
     gemm_avg = sum(gemm_ms) / K
     comb_avg = sum(comb_ms) / K
     peaks, peak_src = load_peaks()
