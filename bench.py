@@ -48,6 +48,8 @@ WORKLOADS = {
                      desc="seeded sampling: H[256,5120] x W[151936,5120] bf16, k=4, GUMBEL_TOKEN T=0.7"),
     "tiny": dict(M=4, d=256, V=4096, k=2, surface="token_logprob",
                  desc="tiny: H[4,256] x W[4096,256] bf16, k=2"),
+    "sampling_token": dict(M=256, d=5120, V=151936, k=4, surface="token_logprob",
+                           desc="256-row decode batch: H[256,5120] x W[151936,5120] bf16, k=4, TOKEN + log-prob"),
     # smaller cases of the same kernels for ncu captures (inputs still larger than L2)
     "decode16_small": dict(M=16, d=1024, V=151936, k=4, surface="token_logprob",
                            desc="profiling case: H[16,1024] x W[151936,1024] bf16, k=4"),

@@ -76,6 +76,8 @@ def lib():
         L.sb_status_string.restype = ctypes.c_char_p
         L.sb_device_info.argtypes = [ctypes.POINTER(i32), ctypes.POINTER(i32)]
         L.sb_device_info.restype = i32
+        L.sb_debug_gumbel_from_bits.argtypes = [P, P, i64, P]
+        L.sb_debug_gumbel_from_bits.restype = i32
         L.sb_debug_configure.argtypes = [i32, u64]
         L.sb_debug_configure.restype = i32
         _lib = L
@@ -151,6 +153,10 @@ def sb_device_info():
     if lib().sb_device_info(ctypes.byref(n), ctypes.byref(cc)) != 0:
         return None
     return n.value, cc.value
+
+
+def sb_debug_gumbel_from_bits(bits, g, count: int, stream=None) -> int:
+    return int(lib().sb_debug_gumbel_from_bits(_ptr(bits), _ptr(g), int(count), _stream(stream)))
 
 
 def sb_debug_configure(stall_epilogue: bool, wait_limit_ns: int) -> int:

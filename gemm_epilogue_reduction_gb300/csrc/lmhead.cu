@@ -16,15 +16,17 @@
 //   warp 1      owns the TMEM allocation; one lane issues tcgen05.mma (M = 128,
 //               bf16 x bf16 -> fp32) into one of two TMEM accumulators and commits
 //               stage releases and "accumulator full" to mbarriers;
-//   warps 2-5   the epilogue: tcgen05.ld of the finished accumulator (warp w reads TMEM
-//               lanes 32*(w%4) .. +31), mask columns outside the tile's shard, fold the
-//               projection record, release the accumulator to the MMA warp.
+//   warps 2-9   the epilogue, two warps per TMEM lane quadrant: tcgen05.ld of the finished
+//               accumulator (warp w reads TMEM lanes 32*(w%4) .. +31), mask columns outside
+//               the tile's shard, fold the projection records, release the accumulator.
 // Two tile orientations share the pipeline:
-//   vocab mode (M <= 256, decode and sampling): A = 128 rows of W (vocabulary), B = all
+//   vocab mode (M <= 128, decode): A = 128 rows of W (vocabulary), B = all
 //               M rows of H (UMMA N = M rounded up to 16).  TMEM lane = vocabulary
 //               column; the epilogue reduces across lanes with warp reductions.
-//   rows mode  (M > 256, prefill scoring): A = 128 rows of H, B = 256 rows of W.
-//               TMEM lane = row of H; each epilogue thread folds its row serially.
+//   rows mode  (M > 128, sampling batches and prefill scoring): A = 128 rows of H, B = 256
+//               rows of W.  TMEM lane = row of H; each epilogue thread folds half of its
+//               row's 256 columns serially.
+// Every record covers 128 vocabulary columns (one vocab-mode tile, half a rows-mode tile).
 // Vocabulary tiles never cross a lane-shard boundary: tile t of shard s starts at
 // s*S + t*TV and is masked at (s+1)*S, so each record belongs to one shard.
 //
@@ -36,6 +38,7 @@
 #include <climits>
 #include <cuda_bf16.h>
 
+#include "sb_gumbel.cuh"
 #include "sb_internal.h"
 #include "sb_ptx.cuh"
 
@@ -78,8 +81,8 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams &p, int tile) {
     TileCoord c;
     const int vt = VOCAB ? tile : tile / p.m_tiles;
     const int mt = VOCAB ? 0 : tile % p.m_tiles;
-    c.s = vt / p.T;
-    c.t = vt - c.s * p.T;
+    c.s = vt / p.Tt;
+    c.t = vt - c.s * p.Tt;
     c.v0 = c.s * p.S + c.t * p.tv;
     c.v_end = min(c.v0 + p.tv, (c.s + 1) * p.S);
     c.m0 = mt * kTileA;
@@ -125,15 +128,15 @@ __device__ __forceinline__ void bwait_drain(uint64_t *bar, uint32_t parity,
     }
 }
 
-__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-// Named-barrier vote over the 128 epilogue threads: true if any thread passes true.
+// Named-barrier vote over the 256 epilogue threads: true if any thread passes true.
 __device__ __forceinline__ bool epi_vote_any(bool pred) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, 1, 128, p;\n\t"
+        "bar.red.or.pred q, 1, 256, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}\n"
         : "=r"(r)
         : "r"(static_cast<uint32_t>(pred))
@@ -141,16 +144,15 @@ __device__ __forceinline__ bool epi_vote_any(bool pred) {
     return r != 0;
 }
 
-// Counter-based Gumbel noise: SplitMix64 (Steele, Lea and Flood, OOPSLA 2014) at stream
-// index n of the stream seeded with `seed` (state seed + (n + 1) * golden increment,
-// then the finaliser), top 24 bits as u in [0, 1), g = -log(-log u) in fp32.
-__device__ __forceinline__ float gumbel_noise(unsigned long long seed, unsigned long long n) {
+// Counter-based uniform: SplitMix64 (Steele, Lea and Flood, OOPSLA 2014) at stream index n
+// of the stream seeded with `seed` (state seed + (n + 1) * golden-ratio increment, then the
+// finaliser); the top 24 bits b give u = b * 2^-24 in [0, 1).
+__device__ __forceinline__ uint32_t uniform_bits24(unsigned long long seed, unsigned long long n) {
     unsigned long long x = seed + (n + 1ull) * 0x9E3779B97F4A7C15ull;
     x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
     x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
     x ^= x >> 31;
-    const float u = static_cast<float>(static_cast<uint32_t>(x >> 40)) * 5.9604644775390625e-8f;
-    return -logf(-logf(u));
+    return static_cast<uint32_t>(x >> 40);
 }
 
 __device__ __forceinline__ uint16_t bf16_bits_rn(float z) {
@@ -159,12 +161,13 @@ __device__ __forceinline__ uint16_t bf16_bits_rn(float z) {
 
 // ------------------------------------------------------------------ epilogue, vocab mode
 // Thread (warp quadrant q, lane) holds vocabulary column v = v0 + 32q + lane for every row
-// (TMEM columns).  Per row: warp max / lowest argmax / sum of exp with warp reductions,
-// then the four warps' partial records merge in quadrant order through shared memory.
+// (TMEM columns).  The two warps of a quadrant take alternate 32-row chunks (half h takes
+// chunks h, h+2, ...).  Per row: warp max / lowest argmax / sum of exp with warp reductions,
+// then the four quadrants' partial records merge in quadrant order through shared memory.
 template <bool GUMBEL, bool FULL>
 __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCoord &c,
                                                uint32_t taddr, uint64_t *tempty_b, int q,
-                                               int lane, const int32_t *tgt_s,
+                                               int h, int lane, const int32_t *tgt_s,
                                                float *scratch) {
     const int nb = p.nb;
     const int v = c.v0 + 32 * q + lane;
@@ -177,18 +180,13 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
     int *sc_gi = reinterpret_cast<int *>(scratch + 16 * nb);
     float *sc_gz = scratch + 20 * nb;
 
-    for (int c0 = 0; c0 < nb; c0 += 32) {
+    for (int c0 = 32 * h; c0 < nb; c0 += 64) {
         uint32_t raw[32];
         const int cw = min(32, nb - c0);
         if (cw == 32)
             tmem_ld32x32b_x32(taddr + c0, raw);
         else
             tmem_ld32x32b_x16(taddr + c0, raw);
-        if (c0 + 32 >= nb) {  // last TMEM read of this tile: hand the accumulator back
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_b);
-        }
         float my_m = -INFINITY, my_s = 0.f, my_gk = -INFINITY, my_gz = 0.f;
         int my_i = INT_MAX, my_gi = INT_MAX;
 #pragma unroll
@@ -205,9 +203,9 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) ws += __shfl_xor_sync(0xFFFFFFFFu, ws, off);
             if (GUMBEL) {
-                const float g = gumbel_noise(
+                const float g = gumbel_from_bits(uniform_bits24(
                     p.seed, static_cast<unsigned long long>(row) * static_cast<unsigned>(p.V) +
-                                static_cast<unsigned>(v));
+                                static_cast<unsigned>(v)));
                 const float key = valid ? y + g : -INFINITY;
                 const uint32_t ok = float_to_ordered(key);
                 const uint32_t okm = __reduce_max_sync(0xFFFFFFFFu, ok);
@@ -240,9 +238,13 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
             }
         }
     }
+    // this warp's TMEM reads of the tile are done: hand its share of the accumulator back
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(tempty_b);
     epi_bar_sync();
     const int te = threadIdx.x - 64;
-    for (int row = te; row < p.M; row += 128) {
+    for (int row = te; row < p.M; row += 32 * kEpiWarps) {
         float m = -INFINITY;
         int idx = INT_MAX;
         for (int w = 0; w < 4; ++w) {
@@ -283,29 +285,32 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
 }
 
 // ------------------------------------------------------------------ epilogue, rows mode
-// Thread (quadrant q, lane) owns row m0 + 32q + lane and walks the tile's 256 columns in
-// chunks of 32: chunk max and first argmax, online rescale of the running sum, then the
-// sum of exp against the running max.
+// Thread (quadrant q, half h, lane) owns row m0 + 32q + lane and the 128 columns
+// [v0 + 128h, v0 + 128h + 128) of the 256-column tile, i.e. record tile 2t + h.  It walks
+// them in chunks of 32: chunk max and first argmax, online rescale of the running sum, then
+// the sum of exp against the running max.
 template <bool GUMBEL, bool FULL>
 __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoord &c,
-                                              uint32_t taddr, uint64_t *tempty_b, int q,
+                                              uint32_t taddr, uint64_t *tempty_b, int q, int h,
                                               int lane) {
     const int row = c.m0 + 32 * q + lane;
     const bool rv = row < p.M;
+    const int rt = 2 * c.t + h;                 // record tile within the shard
+    const int cbase0 = c.v0 + kRecordCols * h;  // first column of this half
     const int tgt = ((p.flags & kFlagTargets) && rv) ? __ldg(p.targets + row) : -1;
     float rm = -INFINITY, rs = 0.f, gk = -INFINITY, gz = 0.f;
     int ri = INT_MAX, gi = INT_MAX;
-    constexpr int kChunks = kRowsTileN / 32;
+    constexpr int kChunks = kRecordCols / 32;
 #pragma unroll 1
     for (int ch = 0; ch < kChunks; ++ch) {
         uint32_t raw[32];
-        tmem_ld32x32b_x32(taddr + ch * 32, raw);
+        tmem_ld32x32b_x32(taddr + kRecordCols * h + ch * 32, raw);
         if (ch == kChunks - 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_b);
         }
-        const int cb = c.v0 + ch * 32;
+        const int cb = cbase0 + ch * 32;
         const int nval = min(32, c.v_end - cb);
         if (nval <= 0) continue;
         float y[32];
@@ -335,7 +340,7 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 if (j < nval) {
-                    const float key = y[j] + gumbel_noise(p.seed, nbase + j);
+                    const float key = y[j] + gumbel_from_bits(uniform_bits24(p.seed, nbase + j));
                     if (key > gk) {
                         gk = key;
                         gi = cb + j;
@@ -371,8 +376,8 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
             }
         }
     }
-    if (rv) {
-        const size_t o = (static_cast<size_t>(row) * p.k + c.s) * p.T + c.t;
+    if (rv && rt < p.T) {
+        const size_t o = (static_cast<size_t>(row) * p.k + c.s) * p.T + rt;
         p.ws.m[o] = rm;
         p.ws.idx[o] = ri;
         p.ws.s[o] = rs;
@@ -418,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], 4);
+            mbar_init(&tempty[i], kEpiWarps);
         }
         mbar_init(drain, 1);
         mbar_init(stall, 1);
@@ -516,8 +521,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ------------------------------------------------ epilogue warps 2..5
-        const int q = warp & 3;
+        // ------------------------------------------------ epilogue warps 2..9
+        const int q = warp & 3;              // TMEM lane quadrant this warp may read
+        const int h = (warp - 2) >> 2;       // which of the quadrant's two warps
         int it = 0;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
             const int b = it & 1;
@@ -533,9 +539,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * p.nb);
             if (VOCAB)
-                epilogue_vocab<GUMBEL, FULL>(p, c, taddr, &tempty[b], q, lane, tgt_s, scratch);
+                epilogue_vocab<GUMBEL, FULL>(p, c, taddr, &tempty[b], q, h, lane, tgt_s, scratch);
             else
-                epilogue_rows<GUMBEL, FULL>(p, c, taddr, &tempty[b], q, lane);
+                epilogue_rows<GUMBEL, FULL>(p, c, taddr, &tempty[b], q, h, lane);
         }
     }
 

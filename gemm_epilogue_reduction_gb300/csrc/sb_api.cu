@@ -76,10 +76,10 @@ bool shape_ok(int64_t M, int64_t V, int32_t k) {
 
 bool vocab_mode(int64_t M) { return M <= kMaxVocabModeRows; }
 
-int32_t tiles_per_shard(int64_t M, int64_t V, int32_t k) {
+// Records per (row, shard): one per 128 vocabulary columns, whatever the tiling.
+int32_t tiles_per_shard(int64_t /*M*/, int64_t V, int32_t k) {
     const int64_t S = V / k;
-    const int64_t tv = vocab_mode(M) ? kVocabTileV : kRowsTileN;
-    return static_cast<int32_t>((S + tv - 1) / tv);
+    return static_cast<int32_t>((S + kRecordCols - 1) / kRecordCols);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
@@ -216,9 +216,10 @@ int32_t enqueue(const void *H, const void *W, int64_t M, int64_t d, int64_t V, i
     p.S = static_cast<int>(V / k);
     p.T = T;
     p.tv = vm ? kVocabTileV : kRowsTileN;
+    p.Tt = static_cast<int>((V / k + p.tv - 1) / p.tv);
     p.nb = vm ? static_cast<int>((M + 15) / 16 * 16) : kRowsTileN;
     p.m_tiles = vm ? 1 : static_cast<int>((M + kTileA - 1) / kTileA);
-    const int64_t tiles = static_cast<int64_t>(k) * T * p.m_tiles;
+    const int64_t tiles = static_cast<int64_t>(k) * p.Tt * p.m_tiles;
     if (tiles >= (int64_t(1) << 31)) return SB_ERR_INVALID_ARG;
     p.num_tiles = static_cast<int>(tiles);
     p.kblocks = static_cast<int>((d + kBlockK - 1) / kBlockK);

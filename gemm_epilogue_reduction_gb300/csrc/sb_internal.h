@@ -11,10 +11,15 @@ constexpr int kBlockK = 64;          // K elements per pipeline stage (one 128-b
 constexpr int kTileA = 128;          // rows of the MMA A operand (the UMMA M)
 constexpr int kRowsTileN = 256;      // vocabulary columns per tile when H rows are the A operand
 constexpr int kVocabTileV = 128;     // vocabulary columns per tile when W rows are the A operand
-constexpr int kMaxVocabModeRows = 256;  // largest M handled with W as the A operand
+constexpr int kRecordCols = 128;     // vocabulary columns covered by one projection record
+#ifndef SB_MAX_VOCAB_MODE_ROWS
+#define SB_MAX_VOCAB_MODE_ROWS 128
+#endif
+constexpr int kMaxVocabModeRows = SB_MAX_VOCAB_MODE_ROWS;  // largest M with W as the A operand
 constexpr int kMaxStages = 16;
 constexpr int kMaxShards = 1024;     // largest k (the combine keeps k shard records in smem)
-constexpr int kThreads = 192;        // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2-5 epilogue
+constexpr int kEpiWarps = 8;         // two epilogue warps per TMEM lane quadrant
+constexpr int kThreads = 32 * (2 + kEpiWarps);  // warp 0 TMA, warp 1 MMA + TMEM, 2-9 epilogue
 constexpr size_t kSmemLimit = 232448;  // 227 KB dynamic shared memory per CTA
 
 // Surface flags the kernels specialise on.
@@ -33,8 +38,9 @@ struct Workspace {       // device views into the caller's workspace
 };
 
 struct GemmParams {
-    int M, d, V, k, S, T;  // T = tiles per shard
-    int tv;                // vocabulary columns per tile
+    int M, d, V, k, S, T;  // T = records per shard (128-column record tiles)
+    int Tt;                // GEMM tiles per shard
+    int tv;                // vocabulary columns per GEMM tile
     int nb;                // rows of the B operand per tile (UMMA N)
     int m_tiles;           // tiles along M (1 when W rows are the A operand)
     int num_tiles;

@@ -104,16 +104,16 @@ typedef struct sb_outputs {
  *   float   gz[n]    SB_GUMBEL_TOKEN only: z at gidx
  *   float   tz[M]    z at target_ids[r] (written only when targets are given)
  * Record (r, s, t) sits at index (r * k + s) * T + t and covers the global columns
- * [s*S + t*TV, min(s*S + (t+1)*TV, (s+1)*S)) with S = V/k and the tile width TV = 128
- * when M <= 256, else 256 (T = ceil(S / TV)).  y is z, or z * (1/T) for SB_GUMBEL_TOKEN
- * with 1/T rounded to fp32 on the host; g is the Gumbel noise of sb_lmhead_project.
+ * [s*S + 128t, min(s*S + 128(t+1), (s+1)*S)) with S = V/k and T = ceil(S / 128).  y is z,
+ * or z * (1/T) for SB_GUMBEL_TOKEN with 1/T rounded to fp32 on the host; g is the Gumbel
+ * noise of sb_lmhead_project.
  */
 
 /* Bytes of workspace one call needs; 0 if the arguments are invalid. */
 size_t sb_workspace_bytes(int64_t M, int64_t V, int32_t k, int32_t surface);
 
-/* Vocabulary tiles per lane shard T used for M rows (the record count per (row, shard));
- * -1 if the arguments are invalid. */
+/* Records per (row, lane shard): T = ceil((V / k) / 128), one per 128 vocabulary columns;
+ * -1 if the arguments are invalid.  (M is accepted for symmetry and does not change T.) */
 int32_t sb_tiles_per_shard(int64_t M, int64_t V, int32_t k);
 
 /*
@@ -131,7 +131,8 @@ int32_t sb_tiles_per_shard(int64_t M, int64_t V, int32_t k);
  *   seed       SB_GUMBEL_TOKEN: the SplitMix64 stream seed.  Column j of row r draws the
  *              output at stream index n = r*V + j, i.e. the SplitMix64 finaliser of
  *              seed + (n + 1) * 0x9E3779B97F4A7C15; u = (x >> 40) * 2^-24 and
- *              g = -log(-log u) in fp32 (u = 0 gives g = -inf).  Ignored otherwise.
+ *              g = -log(-log u) in fp32 to within 2e-6 absolute (u = 0 gives g = -inf).
+ *              Ignored otherwise.
  *   out        outputs and workspace (see sb_outputs); read on the host during the call.
  * Returns SB_OK, or an error with nothing enqueued.
  */
@@ -192,6 +193,11 @@ int32_t sb_lmhead_project_static_scratch(const void *H, const void *W, int64_t M
                                          int64_t V, int32_t k, int32_t surface,
                                          float temperature, uint64_t seed,
                                          const sb_outputs *out, void *stream);
+
+/* Test hook: g[i] = the Gumbel noise the projection kernels derive from the 24-bit
+ * uniform bits[i] & 0xFFFFFF (u = bits * 2^-24), for count entries of device arrays,
+ * enqueued on stream. */
+int32_t sb_debug_gumbel_from_bits(const uint32_t *bits, float *g, int64_t count, void *stream);
 
 /* Device status of the last call that used out->workspace: SB_OK or
  * SB_ERR_DEVICE_TIMEOUT.  Synchronous: copies the header to the host (call it after

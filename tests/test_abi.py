@@ -27,7 +27,7 @@ def _declared():
 
 def test_header_declares_the_entry_points():
     names = _declared()
-    for n in ["sb_workspace_bytes", "sb_tiles_per_shard", "sb_lmhead_project",
+    for n in ["sb_workspace_bytes", "sb_tiles_per_shard", "sb_lmhead_project", "sb_lmhead_records",
               "sb_combine_shard_records", "sb_last_device_status", "sb_status_string"]:
         assert n in names
 
@@ -39,13 +39,12 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_tiles_per_shard_and_workspace_layout():
-    # decode: W rows are the MMA A operand, 128-column vocabulary tiles
+    # one record per 128 vocabulary columns of a shard, whatever the GEMM tiling
     assert sb.sb_tiles_per_shard(16, 151936, 4) == (37984 + 127) // 128 == 297
-    # prefill: 256-column tiles
-    assert sb.sb_tiles_per_shard(4096, 200064, 4) == (50016 + 255) // 256 == 196
+    assert sb.sb_tiles_per_shard(4096, 200064, 4) == (50016 + 127) // 128 == 391
     assert sb.sb_tiles_per_shard(256, 151936, 4) == 297
-    assert sb.sb_tiles_per_shard(257, 151936, 4) == 149
     assert sb.sb_tiles_per_shard(4, 4097, 2) == -1  # V % k != 0
+    assert sb.sb_tiles_per_shard(4, 2048, 1025) == -1  # k above 1024
 
     def al(x):
         return (x + 255) // 256 * 256

@@ -24,10 +24,14 @@ def test_tiny_workload_token_and_logprob():
         run_and_check(4, 256, 4096, 2, surface, targets=True)
 
 
-# (M, d, V, k): vocab mode for M <= 256 (128-column tiles), rows mode above (256-column
-# tiles); tails in M (not a multiple of 16 / 128), d (not a multiple of 64), S (not a
-# multiple of the tile width), single shard, V == k, d == 8.
+# (M, d, V, k): vocab mode for M <= 128 (128-column tiles), rows mode above (256-column
+# tiles, two 128-column records each); tails in M (not a multiple of 16 / 128), d (not a
+# multiple of 64), S (not a multiple of the tile width, S mod 256 below and above 128),
+# single shard, V == k, d == 8.
 SHAPES = [
+    (128, 128, 2048, 2),
+    (129, 64, 2000, 2),
+    (200, 64, 1200, 3),
     (1, 64, 1000, 1),
     (3, 72, 3000, 3),
     (16, 256, 4096, 4),
@@ -65,7 +69,8 @@ def test_full_logits_values_and_tokens(M, d, V, k):
     assert np.array_equal(am[safe], res["token"].cpu().numpy()[safe])
 
 
-@pytest.mark.parametrize("M,d,V,k", [(64, 128, 3000, 3), (300, 64, 2000, 2), (3, 64, 512, 1)])
+@pytest.mark.parametrize("M,d,V,k", [(64, 128, 3000, 3), (300, 64, 2000, 2), (3, 64, 512, 1),
+                                     (256, 128, 3000, 4), (129, 64, 1000, 1)])
 def test_gumbel_sampling_parity(M, d, V, k):
     run_and_check(M, d, V, k, sb.SB_GUMBEL_TOKEN, seed=5, T=0.7, gseed=1234, targets=True)
 
@@ -152,3 +157,22 @@ def test_device_watchdog_reports_timeout_and_context_survives():
     res = sb.project(H, W, k, sb.SB_TOKEN)
     torch.cuda.synchronize()
     assert sb.sb_last_device_status(res["_outputs"]) == sb.SB_OK
+
+
+def test_gumbel_noise_transform_exhaustive_over_all_24bit_uniforms():
+    """The device transform from the 24-bit uniform b to g = -log(-log(b 2^-24)) against
+    the fp64 formula for every one of the 2^24 inputs: within 2e-6 absolute, and -inf at
+    b = 0 only."""
+    import math
+    n = 1 << 24
+    bits = torch.arange(n, dtype=torch.int64, device="cuda").to(torch.int32)
+    g = torch.empty(n, dtype=torch.float32, device="cuda")
+    assert sb.sb_debug_gumbel_from_bits(bits, g, n) == sb.SB_OK
+    torch.cuda.synchronize()
+    got = g.cpu().numpy().astype(np.float64)
+    b = np.arange(n, dtype=np.float64)
+    with np.errstate(divide="ignore"):
+        want = -np.log(-np.log(b / 2.0 ** 24))
+    assert got[0] == -math.inf and np.isfinite(got[1:]).all()
+    err = np.abs(got[1:] - want[1:])
+    assert err.max() <= 2e-6, (float(err.max()), int(err.argmax()) + 1)
