@@ -76,18 +76,22 @@ struct TileCoord {
     int s, t, v0, v_end, m0, a_row, b_row;
 };
 
-template <bool VOCAB>
-__device__ __forceinline__ TileCoord tile_coord(const GemmParams &p, int tile) {
+// Work unit `tile` of a CTA with cluster rank `rank`.  Vocab mode: one 128-column vocabulary
+// tile.  Rows mode: one 256-column vocabulary tile times a group of CS consecutive M tiles,
+// CTA `rank` of the cluster taking M tile CS*group + rank and loading W rows
+// [v0 + rank*256/CS, +256/CS) of the shared W tile (multicast to the whole cluster).
+template <bool VOCAB, int CS>
+__device__ __forceinline__ TileCoord tile_coord(const GemmParams &p, int tile, int rank) {
     TileCoord c;
-    const int vt = VOCAB ? tile : tile / p.m_tiles;
-    const int mt = VOCAB ? 0 : tile % p.m_tiles;
+    const int vt = VOCAB ? tile : tile / p.m_groups;
+    const int mt = VOCAB ? 0 : (tile % p.m_groups) * CS + rank;
     c.s = vt / p.Tt;
     c.t = vt - c.s * p.Tt;
     c.v0 = c.s * p.S + c.t * p.tv;
     c.v_end = min(c.v0 + p.tv, (c.s + 1) * p.S);
     c.m0 = mt * kTileA;
     c.a_row = VOCAB ? c.v0 : c.m0;
-    c.b_row = VOCAB ? 0 : c.v0;
+    c.b_row = VOCAB ? 0 : c.v0 + rank * (kRowsTileN / CS);
     return c;
 }
 
@@ -390,7 +394,7 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
 }
 
 // ------------------------------------------------------------------ the kernel
-template <bool VOCAB, bool GUMBEL, bool FULL>
+template <bool VOCAB, bool GUMBEL, bool FULL, int CS>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const GemmParams p, const uint32_t tmem_cols) {
@@ -415,11 +419,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t b_stage_bytes = static_cast<uint32_t>(p.nb) * 128u;
+    // CTAs of a cluster walk the same work units in lockstep (same stage ring positions):
+    // the W share each loads is multicast into every peer's stage.
+    const int rank = CS > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int unit0 = blockIdx.x / CS;
+    const int unit_stride = gridDim.x / CS;
+    constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CS) - 1u);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+            mbar_init(&empty[i], CS);  // one MMA commit from every CTA of the cluster
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
@@ -441,6 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (CS > 1) cluster_sync();  // peers' barriers are initialised before any multicast
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     // Let the record combine (a programmatic dependent launch) get scheduled early; it
@@ -455,8 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0, issued = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-                const TileCoord c = tile_coord<VOCAB>(p, tile);
+            for (int tile = unit0; ok && tile < p.num_tiles; tile += unit_stride) {
+                const TileCoord c = tile_coord<VOCAB, CS>(p, tile, rank);
                 for (int kb = 0; kb < p.kblocks; ++kb) {
                     if (!bwait(&empty[stage], phase ^ 1u, abort_flag, p)) {
                         ok = false;
@@ -465,8 +476,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(&full[stage], kStageBytesA + b_stage_bytes);
                     tma_load_2d(sA + stage * kStageBytesA, &tmA, &full[stage], kb * kBlockK,
                                 c.a_row, pol_a);
-                    tma_load_2d(sB + stage * b_stage_bytes, &tmB, &full[stage], kb * kBlockK,
-                                c.b_row, pol_b);
+                    if (CS > 1)
+                        tma_load_2d_mc(sB + stage * b_stage_bytes + rank * (b_stage_bytes / CS),
+                                       &tmB, &full[stage], kb * kBlockK, c.b_row, kClusterMask,
+                                       pol_b);
+                    else
+                        tma_load_2d(sB + stage * b_stage_bytes, &tmB, &full[stage], kb * kBlockK,
+                                    c.b_row, pol_b);
                     ++issued;
                     if (++stage == p.stages) {
                         stage = 0;
@@ -488,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             bool ok = true, any = false;
             int it = 0;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+            for (int tile = unit0; ok && tile < p.num_tiles; tile += unit_stride, ++it) {
                 const int b = it & 1;
                 const uint32_t tph = (it >> 1) & 1;
                 if (!bwait(&tempty[b], tph ^ 1u, abort_flag, p)) break;
@@ -506,7 +522,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int ks = 0; ks < kBlockK / 16; ++ks)
                         umma_bf16(d_tmem, adesc + 2u * ks, bdesc + 2u * ks, idesc,
                                   (kb | ks) != 0 ? 1u : 0u);
-                    umma_commit(&empty[stage]);
+                    if (CS > 1)
+                        umma_commit_mc(&empty[stage], kClusterMask);  // frees it cluster-wide
+                    else
+                        umma_commit(&empty[stage]);
                     any = true;
                     if (++stage == p.stages) {
                         stage = 0;
@@ -525,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;              // TMEM lane quadrant this warp may read
         const int h = (warp - 2) >> 2;       // which of the quadrant's two warps
         int it = 0;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+        for (int tile = unit0; tile < p.num_tiles; tile += unit_stride, ++it) {
             const int b = it & 1;
             const uint32_t tph = (it >> 1) & 1;
             bool ok;
@@ -535,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = bwait(&tfull[b], tph, abort_flag, p);
             if (epi_vote_any(!ok)) break;
             tc_fence_after();
-            const TileCoord c = tile_coord<VOCAB>(p, tile);
+            const TileCoord c = tile_coord<VOCAB, CS>(p, tile, rank);
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * p.nb);
             if (VOCAB)
@@ -547,6 +566,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    // Every role has drained what it issued (its TMA copies, its MMAs and their commits to
+    // the peers); wait until the peers have too, so nothing lands here after exit.
+    if (CS > 1) cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -554,10 +576,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool VOCAB, bool GUMBEL, bool FULL>
+template <bool VOCAB, bool GUMBEL, bool FULL, int CS>
 cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p,
-                     int grid, size_t smem, cudaStream_t stream) {
-    auto kern = lmhead_kernel<VOCAB, GUMBEL, FULL>;
+                     size_t smem, int num_sms, cudaStream_t stream) {
+    auto kern = lmhead_kernel<VOCAB, GUMBEL, FULL, CS>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -566,8 +588,29 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmP
         cols = 32;
         while (cols < static_cast<uint32_t>(2 * p.nb)) cols <<= 1;
     }
-    kern<<<grid, kThreads, smem, stream>>>(tmA, tmB, p, cols);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // persistent grid: as many clusters as can be resident at once (one CTA per SM)
+    int clusters = num_sms / CS;
+    if (CS > 1) {
+        cfg.gridDim = dim3(CS * clusters);
+        int active = 0;
+        if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) == cudaSuccess && active > 0)
+            clusters = active < clusters ? active : clusters;
+    }
+    if (clusters > p.num_tiles) clusters = p.num_tiles;
+    if (clusters < 1) clusters = 1;
+    cfg.gridDim = dim3(CS * clusters);
+    return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p, cols);
 }
 
 }  // namespace
@@ -583,19 +626,20 @@ int lmhead_max_stages(int nb, bool vocab_mode, int flags) {
 }
 
 cudaError_t launch_lmhead(bool vocab_mode, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                          const GemmParams &p, int grid, size_t smem, cudaStream_t stream) {
+                          const GemmParams &p, size_t smem, int num_sms, cudaStream_t stream) {
     const bool g = (p.flags & kFlagGumbel) != 0;
     const bool f = (p.flags & kFlagFull) != 0;
     if (vocab_mode) {
-        if (g) return f ? launch_t<true, true, true>(tmA, tmB, p, grid, smem, stream)
-                        : launch_t<true, true, false>(tmA, tmB, p, grid, smem, stream);
-        return f ? launch_t<true, false, true>(tmA, tmB, p, grid, smem, stream)
-                 : launch_t<true, false, false>(tmA, tmB, p, grid, smem, stream);
+        if (g) return f ? launch_t<true, true, true, 1>(tmA, tmB, p, smem, num_sms, stream)
+                        : launch_t<true, true, false, 1>(tmA, tmB, p, smem, num_sms, stream);
+        return f ? launch_t<true, false, true, 1>(tmA, tmB, p, smem, num_sms, stream)
+                 : launch_t<true, false, false, 1>(tmA, tmB, p, smem, num_sms, stream);
     }
-    if (g) return f ? launch_t<false, true, true>(tmA, tmB, p, grid, smem, stream)
-                    : launch_t<false, true, false>(tmA, tmB, p, grid, smem, stream);
-    return f ? launch_t<false, false, true>(tmA, tmB, p, grid, smem, stream)
-             : launch_t<false, false, false>(tmA, tmB, p, grid, smem, stream);
+    constexpr int C = kRowsCluster;
+    if (g) return f ? launch_t<false, true, true, C>(tmA, tmB, p, smem, num_sms, stream)
+                    : launch_t<false, true, false, C>(tmA, tmB, p, smem, num_sms, stream);
+    return f ? launch_t<false, false, true, C>(tmA, tmB, p, smem, num_sms, stream)
+             : launch_t<false, false, false, C>(tmA, tmB, p, smem, num_sms, stream);
 }
 
 }  // namespace sb

@@ -219,7 +219,9 @@ int32_t enqueue(const void *H, const void *W, int64_t M, int64_t d, int64_t V, i
     p.Tt = static_cast<int>((V / k + p.tv - 1) / p.tv);
     p.nb = vm ? static_cast<int>((M + 15) / 16 * 16) : kRowsTileN;
     p.m_tiles = vm ? 1 : static_cast<int>((M + kTileA - 1) / kTileA);
-    const int64_t tiles = static_cast<int64_t>(k) * p.Tt * p.m_tiles;
+    p.cluster = vm ? 1 : kRowsCluster;
+    p.m_groups = (p.m_tiles + p.cluster - 1) / p.cluster;
+    const int64_t tiles = static_cast<int64_t>(k) * p.Tt * p.m_groups;
     if (tiles >= (int64_t(1) << 31)) return SB_ERR_INVALID_ARG;
     p.num_tiles = static_cast<int>(tiles);
     p.kblocks = static_cast<int>((d + kBlockK - 1) / kBlockK);
@@ -235,13 +237,14 @@ int32_t enqueue(const void *H, const void *W, int64_t M, int64_t d, int64_t V, i
     p.debug_stall = g_debug_stall.load();
 
     CUtensorMap tmA, tmB;
+    // rows mode: each CTA of a cluster loads 256 / cluster rows of the shared W tile
     const bool ok = vm ? (make_map(&tmA, W, V, d, kTileA) && make_map(&tmB, H, M, d, p.nb))
-                       : (make_map(&tmA, H, M, d, kTileA) && make_map(&tmB, W, V, d, kRowsTileN));
+                       : (make_map(&tmA, H, M, d, kTileA) &&
+                          make_map(&tmB, W, V, d, kRowsTileN / p.cluster));
     if (!ok) return SB_ERR_CUDA;
-    const int grid = static_cast<int>(tiles < dev.sms ? tiles : dev.sms);
     const size_t smem = lmhead_smem_bytes(p.nb, p.stages, vm, flags);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (launch_lmhead(vm, tmA, tmB, p, grid, smem, st) != cudaSuccess) return SB_ERR_CUDA;
+    if (launch_lmhead(vm, tmA, tmB, p, smem, dev.sms, st) != cudaSuccess) return SB_ERR_CUDA;
     if (!with_combine) return SB_OK;
     const CombineParams c = combine_params(out, p.ws, M, k, T, flags, inv_t);
     if (launch_combine(c, st) != cudaSuccess) return SB_ERR_CUDA;

@@ -17,7 +17,8 @@ constexpr int kRecordCols = 128;     // vocabulary columns covered by one projec
 #endif
 constexpr int kMaxVocabModeRows = SB_MAX_VOCAB_MODE_ROWS;  // largest M with W as the A operand
 constexpr int kMaxStages = 16;
-constexpr int kMaxShards = 1024;     // largest k (the combine keeps k shard records in smem)
+constexpr int kMaxShards = 1024;
+constexpr int kRowsCluster = 2;      // rows mode: CTAs (consecutive M tiles) sharing a W tile     // largest k (the combine keeps k shard records in smem)
 constexpr int kEpiWarps = 8;         // two epilogue warps per TMEM lane quadrant
 constexpr int kThreads = 32 * (2 + kEpiWarps);  // warp 0 TMA, warp 1 MMA + TMEM, 2-9 epilogue
 constexpr size_t kSmemLimit = 232448;  // 227 KB dynamic shared memory per CTA
@@ -43,6 +44,8 @@ struct GemmParams {
     int tv;                // vocabulary columns per GEMM tile
     int nb;                // rows of the B operand per tile (UMMA N)
     int m_tiles;           // tiles along M (1 when W rows are the A operand)
+    int m_groups;          // groups of `cluster` consecutive M tiles (rows mode)
+    int cluster;           // CTAs per cluster sharing each W tile (1 or 2)
     int num_tiles;
     int kblocks;
     int stages;
@@ -70,7 +73,7 @@ struct CombineParams {
 
 // Launchers (lmhead.cu, combine.cu).  Return cudaSuccess or the launch error.
 cudaError_t launch_lmhead(bool vocab_mode, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                          const GemmParams &p, int grid, size_t smem, cudaStream_t stream);
+                          const GemmParams &p, size_t smem, int num_sms, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
 
 size_t lmhead_smem_bytes(int nb, int stages, bool vocab_mode, int flags);

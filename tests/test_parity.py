@@ -140,10 +140,12 @@ def test_token_surface_leaves_a_logits_buffer_untouched():
     assert bool((sentinel == 12345).all())
 
 
-def test_device_watchdog_reports_timeout_and_context_survives():
+@pytest.mark.parametrize("M", [16, 300])
+def test_device_watchdog_reports_timeout_and_context_survives(M):
     """A wait that nothing will satisfy runs out after the configured limit; the kernel
-    records SB_ERR_DEVICE_TIMEOUT, releases TMEM and exits; the next call is correct."""
-    M, d, V, k = 16, 128, 2048, 2
+    records SB_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, releases TMEM and exits (for
+    M = 300 inside 2-CTA clusters); the next call is correct."""
+    d, V, k = 128, 2048, 2
     H, W = synth.make_hw(M, d, V, seed=2)
     H, W = H.cuda(), W.cuda()
     try:
