@@ -11,12 +11,13 @@
 // Structure (the warp roles and TMEM epilogue of the "01 · 通算融合" note on Blackwell
 // SM100 GEMMs, sections 2 and 5.1: TMA producer, MMA issuer, epilogue warps; full-K
 // accumulation before any epilogue work):
-//   warp 0      one lane issues TMA loads of 64-wide K slices of both operands into a
-//               ring of shared-memory stages (128-byte swizzle);
+//   warps 0, 2  one lane each issues TMA loads of 64-wide K slices of one operand into its
+//               own ring of shared-memory stages (128-byte swizzle); the ring of the
+//               operand streamed from HBM (W) is deeper than the one re-read from L2 (H);
 //   warp 1      owns the TMEM allocation; one lane issues tcgen05.mma (M = 128,
 //               bf16 x bf16 -> fp32) into one of two TMEM accumulators and commits
 //               stage releases and "accumulator full" to mbarriers;
-//   warps 2-9   the epilogue, two warps per TMEM lane quadrant: tcgen05.ld of the finished
+//   warps 3-10  the epilogue, two warps per TMEM lane quadrant: tcgen05.ld of the finished
 //               accumulator (warp w reads TMEM lanes 32*(w%4) .. +31), mask columns outside
 //               the tile's shard, fold the projection records, release the accumulator.
 // Two tile orientations share the pipeline:
@@ -53,15 +54,18 @@ struct SmemLayout {
     uint32_t a_off, b_off, bar_off, misc_off, tgt_off, scratch_off, total;
 };
 
-__host__ __device__ inline SmemLayout make_layout(int nb, int stages, bool vocab, int flags) {
+// Shared memory: ring A (stages_a x 16 KB), ring B (stages_b x nb*128 B), mbarriers,
+// TMEM address + abort flag, vocab-mode target ids and cross-quadrant scratch.
+__host__ __device__ inline SmemLayout make_layout(int nb, int stages_a, int stages_b, bool vocab,
+                                                  int flags) {
     SmemLayout L;
     uint32_t off = 0;
     L.a_off = off;
-    off += stages * kStageBytesA;
+    off += stages_a * kStageBytesA;
     L.b_off = off;
-    off += stages * nb * 128;
+    off += stages_b * nb * 128;
     L.bar_off = off;
-    off += (2 * kMaxStages + 8) * 8;
+    off += (4 * kMaxStages + 8) * 8;
     L.misc_off = off;
     off += 16;
     L.tgt_off = off;
@@ -247,7 +251,7 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
     __syncwarp();
     if (lane == 0) mbar_arrive(tempty_b);
     epi_bar_sync();
-    const int te = threadIdx.x - 64;
+    const int te = threadIdx.x - 32 * kFirstEpiWarp;
     for (int row = te; row < p.M; row += 32 * kEpiWarps) {
         float m = -INFINITY;
         int idx = INT_MAX;
@@ -394,6 +398,54 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
 }
 
 // ------------------------------------------------------------------ the kernel
+// One producer per operand ring, so the operand streamed from HBM (W) can run further ahead
+// of the MMA than the one re-read from L2 (H).
+template <int NSTAGES_MAX>
+__device__ __forceinline__ void produce_ring(const GemmParams &p, const CUtensorMap *tm,
+                                             uint8_t *ring, uint32_t stage_bytes, int stages,
+                                             uint64_t *full, uint64_t *empty, bool is_a,
+                                             bool multicast, int rank, int cs, uint16_t mask,
+                                             uint64_t policy, int unit0, int unit_stride,
+                                             bool vocab, volatile int *abort_flag,
+                                             TileCoord (*coord)(const GemmParams &, int, int)) {
+    int stage = 0;
+    uint32_t phase = 0, issued = 0;
+    bool ok = true;
+    for (int tile = unit0; ok && tile < p.num_tiles; tile += unit_stride) {
+        const TileCoord c = coord(p, tile, rank);
+        const int row = is_a ? c.a_row : c.b_row;
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+            if (!bwait(&empty[stage], phase ^ 1u, abort_flag, p)) {
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx(&full[stage], stage_bytes);
+            uint8_t *dst = ring + stage * stage_bytes;
+            if (multicast)
+                tma_load_2d_mc(dst + rank * (stage_bytes / cs), tm, &full[stage], kb * kBlockK,
+                               row, mask, policy);
+            else
+                tma_load_2d(dst, tm, &full[stage], kb * kBlockK, row, policy);
+            ++issued;
+            if (++stage == stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    // Drain: the last `stages` issues may still be landing (only possible after an abort;
+    // on the normal path the MMA warp consumed every one of them).  A stage's barrier also
+    // counts the bytes a cluster peer multicasts into it.
+    const uint32_t n = issued < static_cast<uint32_t>(stages) ? issued : stages;
+    for (uint32_t i = issued - n; i < issued; ++i)
+        bwait_drain(&full[i % stages], (i / stages) & 1u, abort_flag, p);
+}
+
+template <bool VOCAB, int CS>
+__device__ TileCoord coord_fn(const GemmParams &p, int tile, int rank) {
+    return tile_coord<VOCAB, CS>(p, tile, rank);
+}
+
 template <bool VOCAB, bool GUMBEL, bool FULL, int CS>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -401,13 +453,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    const SmemLayout L = make_layout(p.nb, p.stages, VOCAB, p.flags);
+    const SmemLayout L = make_layout(p.nb, p.stages_a, p.stages_b, VOCAB, p.flags);
     uint8_t *sA = smem + L.a_off;
     uint8_t *sB = smem + L.b_off;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
-    uint64_t *full = bars;
-    uint64_t *empty = bars + kMaxStages;
-    uint64_t *tfull = bars + 2 * kMaxStages;
+    uint64_t *fullA = bars;
+    uint64_t *emptyA = bars + kMaxStages;
+    uint64_t *fullB = bars + 2 * kMaxStages;
+    uint64_t *emptyB = bars + 3 * kMaxStages;
+    uint64_t *tfull = bars + 4 * kMaxStages;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
     uint64_t *stall = drain + 1;
@@ -419,17 +473,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t b_stage_bytes = static_cast<uint32_t>(p.nb) * 128u;
-    // CTAs of a cluster walk the same work units in lockstep (same stage ring positions):
-    // the W share each loads is multicast into every peer's stage.
+    // CTAs of a cluster walk the same work units in lockstep (same B-ring positions): the
+    // W share each loads is multicast into every peer's B stage.
     const int rank = CS > 1 ? static_cast<int>(cluster_ctarank()) : 0;
     const int unit0 = blockIdx.x / CS;
     const int unit_stride = gridDim.x / CS;
     constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CS) - 1u);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < p.stages; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], CS);  // one MMA commit from every CTA of the cluster
+        for (int i = 0; i < p.stages_a; ++i) {
+            mbar_init(&fullA[i], 1);
+            mbar_init(&emptyA[i], 1);
+        }
+        for (int i = 0; i < p.stages_b; ++i) {
+            mbar_init(&fullB[i], 1);
+            mbar_init(&emptyB[i], CS);  // one MMA commit from every CTA of the cluster
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
@@ -458,50 +516,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     // waits for this whole grid to finish before it reads any record.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    if (warp == 0) {
-        // ------------------------------------------------ TMA producer (one lane)
+    if (warp == 0 || warp == 2) {
+        // ------------------------------------------------ TMA producers (one lane each):
+        // warp 0 fills ring A, warp 2 ring B.  W is streamed once (evict first in vocab
+        // mode); H and shared W tiles are re-read from L2.
         if (lane == 0) {
-            const uint64_t pol_a = VOCAB ? policy_evict_first() : policy_evict_last();
-            const uint64_t pol_b = VOCAB ? policy_evict_last() : policy_evict_normal();
-            int stage = 0;
-            uint32_t phase = 0, issued = 0;
-            bool ok = true;
-            for (int tile = unit0; ok && tile < p.num_tiles; tile += unit_stride) {
-                const TileCoord c = tile_coord<VOCAB, CS>(p, tile, rank);
-                for (int kb = 0; kb < p.kblocks; ++kb) {
-                    if (!bwait(&empty[stage], phase ^ 1u, abort_flag, p)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&full[stage], kStageBytesA + b_stage_bytes);
-                    tma_load_2d(sA + stage * kStageBytesA, &tmA, &full[stage], kb * kBlockK,
-                                c.a_row, pol_a);
-                    if (CS > 1)
-                        tma_load_2d_mc(sB + stage * b_stage_bytes + rank * (b_stage_bytes / CS),
-                                       &tmB, &full[stage], kb * kBlockK, c.b_row, kClusterMask,
-                                       pol_b);
-                    else
-                        tma_load_2d(sB + stage * b_stage_bytes, &tmB, &full[stage], kb * kBlockK,
-                                    c.b_row, pol_b);
-                    ++issued;
-                    if (++stage == p.stages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            // Drain: the last `stages` issues may still be landing (only possible after an
-            // abort; on the normal path the MMA warp consumed every one of them).
-            const uint32_t n = issued < static_cast<uint32_t>(p.stages) ? issued : p.stages;
-            for (uint32_t i = issued - n; i < issued; ++i)
-                bwait_drain(&full[i % p.stages], (i / p.stages) & 1u, abort_flag, p);
+            if (warp == 0)
+                produce_ring<kMaxStages>(p, &tmA, sA, kStageBytesA, p.stages_a, fullA, emptyA,
+                                         true, false, rank, CS, kClusterMask,
+                                         VOCAB ? policy_evict_first() : policy_evict_last(),
+                                         unit0, unit_stride, VOCAB, abort_flag,
+                                         coord_fn<VOCAB, CS>);
+            else
+                produce_ring<kMaxStages>(p, &tmB, sB, b_stage_bytes, p.stages_b, fullB, emptyB,
+                                         false, CS > 1, rank, CS, kClusterMask,
+                                         VOCAB ? policy_evict_last() : policy_evict_normal(),
+                                         unit0, unit_stride, VOCAB, abort_flag,
+                                         coord_fn<VOCAB, CS>);
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (one lane)
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(kTileA, p.nb);
-            int stage = 0;
-            uint32_t phase = 0;
+            int sa = 0, sb = 0;
+            uint32_t pa = 0, pb = 0;
             bool ok = true, any = false;
             int it = 0;
             for (int tile = unit0; ok && tile < p.num_tiles; tile += unit_stride, ++it) {
@@ -511,25 +549,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * p.nb);
                 for (int kb = 0; kb < p.kblocks; ++kb) {
-                    if (!bwait(&full[stage], phase, abort_flag, p)) {
+                    if (!bwait(&fullA[sa], pa, abort_flag, p) ||
+                        !bwait(&fullB[sb], pb, abort_flag, p)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * kStageBytesA));
-                    const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * b_stage_bytes));
+                    const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + sa * kStageBytesA));
+                    const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + sb * b_stage_bytes));
 #pragma unroll
                     for (int ks = 0; ks < kBlockK / 16; ++ks)
                         umma_bf16(d_tmem, adesc + 2u * ks, bdesc + 2u * ks, idesc,
                                   (kb | ks) != 0 ? 1u : 0u);
+                    umma_commit(&emptyA[sa]);
                     if (CS > 1)
-                        umma_commit_mc(&empty[stage], kClusterMask);  // frees it cluster-wide
+                        umma_commit_mc(&emptyB[sb], kClusterMask);  // frees it cluster-wide
                     else
-                        umma_commit(&empty[stage]);
+                        umma_commit(&emptyB[sb]);
                     any = true;
-                    if (++stage == p.stages) {
-                        stage = 0;
-                        phase ^= 1u;
+                    if (++sa == p.stages_a) {
+                        sa = 0;
+                        pa ^= 1u;
+                    }
+                    if (++sb == p.stages_b) {
+                        sb = 0;
+                        pb ^= 1u;
                     }
                 }
                 if (ok) umma_commit(&tfull[b]);
@@ -540,9 +584,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ------------------------------------------------ epilogue warps 2..9
+        // ------------------------------------------------ epilogue warps 3..10
         const int q = warp & 3;              // TMEM lane quadrant this warp may read
-        const int h = (warp - 2) >> 2;       // which of the quadrant's two warps
+        const int h = (warp - 3) >> 2;       // which of the quadrant's two warps
         int it = 0;
         for (int tile = unit0; tile < p.num_tiles; tile += unit_stride, ++it) {
             const int b = it & 1;
@@ -615,14 +659,8 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmP
 
 }  // namespace
 
-size_t lmhead_smem_bytes(int nb, int stages, bool vocab_mode, int flags) {
-    return make_layout(nb, stages, vocab_mode, flags).total;
-}
-
-int lmhead_max_stages(int nb, bool vocab_mode, int flags) {
-    int s = kMaxStages;
-    while (s > 1 && make_layout(nb, s, vocab_mode, flags).total > kSmemLimit) --s;
-    return s;
+size_t lmhead_smem_bytes(int nb, int stages_a, int stages_b, bool vocab_mode, int flags) {
+    return make_layout(nb, stages_a, stages_b, vocab_mode, flags).total;
 }
 
 cudaError_t launch_lmhead(bool vocab_mode, const CUtensorMap &tmA, const CUtensorMap &tmB,

@@ -18,9 +18,13 @@ constexpr int kRecordCols = 128;     // vocabulary columns covered by one projec
 constexpr int kMaxVocabModeRows = SB_MAX_VOCAB_MODE_ROWS;  // largest M with W as the A operand
 constexpr int kMaxStages = 16;
 constexpr int kMaxShards = 1024;
-constexpr int kRowsCluster = 2;      // rows mode: CTAs (consecutive M tiles) sharing a W tile     // largest k (the combine keeps k shard records in smem)
+#ifndef SB_ROWS_CLUSTER
+#define SB_ROWS_CLUSTER 2
+#endif
+constexpr int kRowsCluster = SB_ROWS_CLUSTER;  // rows mode: CTAs (consecutive M tiles) per W tile     // largest k (the combine keeps k shard records in smem)
 constexpr int kEpiWarps = 8;         // two epilogue warps per TMEM lane quadrant
-constexpr int kThreads = 32 * (2 + kEpiWarps);  // warp 0 TMA, warp 1 MMA + TMEM, 2-9 epilogue
+constexpr int kFirstEpiWarp = 3;     // warps 0 and 2 load, warp 1 issues MMAs + owns TMEM
+constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
 constexpr size_t kSmemLimit = 232448;  // 227 KB dynamic shared memory per CTA
 
 // Surface flags the kernels specialise on.
@@ -48,7 +52,8 @@ struct GemmParams {
     int cluster;           // CTAs per cluster sharing each W tile (1 or 2)
     int num_tiles;
     int kblocks;
-    int stages;
+    int stages_a;          // ring depth of the UMMA A operand (16 KB stages)
+    int stages_b;          // ring depth of the UMMA B operand (nb * 128 B stages)
     int flags;
     float inv_t;
     unsigned long long seed;
@@ -76,7 +81,6 @@ cudaError_t launch_lmhead(bool vocab_mode, const CUtensorMap &tmA, const CUtenso
                           const GemmParams &p, size_t smem, int num_sms, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
 
-size_t lmhead_smem_bytes(int nb, int stages, bool vocab_mode, int flags);
-int lmhead_max_stages(int nb, bool vocab_mode, int flags);
+size_t lmhead_smem_bytes(int nb, int stages_a, int stages_b, bool vocab_mode, int flags);
 
 }  // namespace sb
