@@ -66,9 +66,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # dram__bytes_write.sum), with the hash of the kernel source it was taken on; reported as
 # null once the source differs.
 KERNEL_TRAFFIC = {
-    # decode16: --set full capture of the d=1024 case of the same kernel (reads 311.34 MB for
-    # 311.20 MB of W + H, writes 3.28 MB), reads scaled by 5x to d=5120.
-    "decode16": {"bytes": 1.5600e9, "src_sha": "b7ea8294071aa7ff"},
+    # decode16: dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
+    # (1,556,163,072 + 3,185,664 B; W + H are 1,555,988,480 B).
+    "decode16": {"bytes": 1559348736, "src_sha": "29e05b26d955f669"},
 }
 
 
