@@ -33,12 +33,18 @@ struct GRec {
     float z;
 };
 
+__device__ __forceinline__ float exp_nonpos(float x) {  // e^x for x <= 0 (2 ulp)
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * 1.4426950408889634f));
+    return y;
+}
+
 __device__ __forceinline__ Rec merge(const Rec &a, const Rec &b) {
     Rec r;
     r.m = fmaxf(a.m, b.m);
     r.i = (a.m > b.m) ? a.i : ((b.m > a.m) ? b.i : min(a.i, b.i));
-    const float sa = (a.m == -INFINITY) ? 0.f : a.s * expf(a.m - r.m);
-    const float sb = (b.m == -INFINITY) ? 0.f : b.s * expf(b.m - r.m);
+    const float sa = (a.m == -INFINITY) ? 0.f : a.s * exp_nonpos(a.m - r.m);
+    const float sb = (b.m == -INFINITY) ? 0.f : b.s * exp_nonpos(b.m - r.m);
     r.s = sa + sb;
     return r;
 }
@@ -48,7 +54,7 @@ __device__ __forceinline__ GRec gmerge(const GRec &a, const GRec &b) {
 }
 
 constexpr int kMaxWarps = 8;
-constexpr int kBatch = 8;  // records each lane loads before folding them
+constexpr int kBatch = 16;  // records each lane loads before folding them
 
 // One block per row; warp w completes shards w, w + 8, ... (lane l folds tiles l, l+32, ...
 // in ascending order, loading kBatch of them at a time, then the xor butterfly), writes the

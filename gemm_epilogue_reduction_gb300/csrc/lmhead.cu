@@ -35,6 +35,7 @@
 // out records SB_ERR_DEVICE_TIMEOUT in the workspace status word, raises a CTA-wide abort
 // flag, and every role then drains its own in-flight TMA copies and MMAs before the TMEM
 // is freed and the CTA exits.
+#include <atomic>
 #include <cfloat>
 #include <climits>
 #include <cuda_bf16.h>
@@ -624,9 +625,18 @@ template <bool VOCAB, bool GUMBEL, bool FULL, int CS>
 cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p,
                      size_t smem, int num_sms, cudaStream_t stream) {
     auto kern = lmhead_kernel<VOCAB, GUMBEL, FULL, CS>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // The shared-memory opt-in is per device; every launch asks for at most kSmemLimit.
+    static std::atomic<uint64_t> opted_in{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+    if (!bit || !(opted_in.load() & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemLimit));
+        if (e != cudaSuccess) return e;
+        opted_in.fetch_or(bit);
+    }
     uint32_t cols = 512;
     if (VOCAB) {
         cols = 32;
@@ -646,10 +656,18 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmP
     // persistent grid: as many clusters as can be resident at once (one CTA per SM)
     int clusters = num_sms / CS;
     if (CS > 1) {
-        cfg.gridDim = dim3(CS * clusters);
-        int active = 0;
-        if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) == cudaSuccess && active > 0)
-            clusters = active < clusters ? active : clusters;
+        // co-resident clusters (GPCs may not pair every SM); queried once per device for the
+        // largest shared-memory footprint this kernel is launched with
+        static std::atomic<int> active_by_dev[64];
+        int active = (dev < 64) ? active_by_dev[dev].load() : 0;
+        if (active <= 0) {
+            cudaLaunchConfig_t q = cfg;
+            q.gridDim = dim3(CS * clusters);
+            q.dynamicSmemBytes = kSmemLimit;
+            if (cudaOccupancyMaxActiveClusters(&active, kern, &q) != cudaSuccess) active = 0;
+            if (active > 0 && dev < 64) active_by_dev[dev].store(active);
+        }
+        if (active > 0) clusters = active < clusters ? active : clusters;
     }
     if (clusters > p.num_tiles) clusters = p.num_tiles;
     if (clusters < 1) clusters = 1;

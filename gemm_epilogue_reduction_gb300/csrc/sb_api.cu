@@ -96,19 +96,45 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     return fn;
 }
 
+// A few recently encoded maps, keyed by everything the encoding depends on (a map holds no
+// device state, so reusing one for the same pointer and shape is exact).
+struct MapCacheEntry {
+    const void *base;
+    int64_t rows, d;
+    int box_rows;
+    CUtensorMap map;
+    bool used;
+};
+constexpr int kMapCache = 16;
+std::mutex g_map_mu;
+MapCacheEntry g_map_cache[kMapCache];
+int g_map_next = 0;
+
 // 2-D map over a row-major bf16 matrix [rows, d]: boxes of 64 x box_rows, 128-byte swizzle,
 // out-of-range elements read as zero.
 bool make_map(CUtensorMap *tm, const void *base, int64_t rows, int64_t d, int box_rows) {
+    {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        for (const auto &e : g_map_cache)
+            if (e.used && e.base == base && e.rows == rows && e.d == d && e.box_rows == box_rows) {
+                *tm = e.map;
+                return true;
+            }
+    }
     auto enc = encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t es[2] = {1, 1};
-    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    if (enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    g_map_cache[g_map_next] = MapCacheEntry{base, rows, d, box_rows, *tm, true};
+    g_map_next = (g_map_next + 1) % kMapCache;
+    return true;
 }
 
 struct DevInfo {
