@@ -70,6 +70,8 @@ def _load():
         lib.oracle_project.argtypes = [P, P, P, i64, i64, i64, i32, i32, f64, u64, P,
                                        P, P, P, P, P, P, P, P, P, P]
         lib.oracle_project.restype = ctypes.c_int
+        lib.oracle_topk.argtypes = [P, P, i64, i64, i64, i32, P, P, P]
+        lib.oracle_topk.restype = ctypes.c_int
         lib.oracle_payload_bytes_per_row.argtypes = [i32, i64]
         lib.oracle_payload_bytes_per_row.restype = f64
         _lib = lib
@@ -128,6 +130,21 @@ def selection_key(z: float, row: int, col: int, V: int, gumbel: bool = False,
 
 def payload_bytes_per_row(surface: int, V: int) -> float:
     return float(_load().oracle_payload_bytes_per_row(int(surface), int(V)))
+
+
+def topk(H_bits, W_bits, K: int) -> dict:
+    """Top-K log-probability surface of every row (see ``oracle_topk`` in oracle.c):
+    ids [M, K] (logit descending, ties to the lower column), logprob [M, K], lse [M]."""
+    H, W = _bits(H_bits), _bits(W_bits)
+    M, d = H.shape
+    V, d2 = W.shape
+    assert d == d2
+    out = {"ids": np.empty((M, K), np.int32), "logprob": np.empty((M, K)), "lse": np.empty(M)}
+    rc = _load().oracle_topk(_ptr(H), _ptr(W), M, d, V, int(K), _ptr(out["ids"]),
+                             _ptr(out["logprob"]), _ptr(out["lse"]))
+    if rc != 0:
+        raise ValueError("oracle_topk rejected its arguments")
+    return out
 
 
 def project(H_bits, W_bits, k: int, *, gumbel: bool = False, temperature: float = 1.0,

@@ -247,6 +247,45 @@ int oracle_project(const uint16_t *H, const uint16_t *W, const int64_t *row_ids,
 }
 
 /*
+ * Top-K log-probability surface (a "registered projection" in the sense of Section 2.2:
+ * the log-probabilities of the K most likely tokens instead of all V): per row, the K
+ * columns with the largest logits, ordered by logit descending and, among equal logits, by
+ * column ascending (the deterministic tie rule of Section 3.1), each with its natural-log
+ * log-probability z_j - lse.  Selection is K passes of "lowest index attaining the maximum
+ * among the columns not yet taken".  ids [M][K], logprob [M][K], lse [M] (NULL allowed).
+ * Returns 0, or -1 on invalid arguments (K < 1 or K > V).
+ */
+int oracle_topk(const uint16_t *H, const uint16_t *W, int64_t M, int64_t d, int64_t V,
+                int32_t K, int32_t *ids, double *logprob, double *lse_out) {
+    if (M < 1 || d < 1 || V < 1 || K < 1 || K > V) return -1;
+    double *z = (double *)malloc(sizeof(double) * (size_t)(M * V));
+    if (!z) return -1;
+    oracle_logits(H, W, M, d, V, z);
+#pragma omp parallel
+    {
+        unsigned char *taken = (unsigned char *)malloc((size_t)V);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < M; ++r) {
+            const double *zr = z + r * V;
+            const double l = lse_range(zr, 0, V);
+            if (lse_out) lse_out[r] = l;
+            memset(taken, 0, (size_t)V);
+            for (int32_t q = 0; q < K; ++q) {
+                int64_t best = -1;
+                for (int64_t j = 0; j < V; ++j)
+                    if (!taken[j] && (best < 0 || zr[j] > zr[best])) best = j;
+                taken[best] = 1;
+                ids[r * K + q] = (int32_t)best;
+                logprob[r * K + q] = zr[best] - l;
+            }
+        }
+        free(taken);
+    }
+    free(z);
+    return 0;
+}
+
+/*
  * Result bytes a consumer receives per row: the token surface carries one int32
  * ID, the complete-logit surface carries V bf16 logits (the payload contrast of
  * Figure 1 and Figure 3a: k int32 IDs instead of V logit elements).

@@ -28,6 +28,10 @@ MUTATIONS = {
                                    "return z * temperature + oracle_gumbel"),
     "uniform_wrong_shift": ("(oracle_splitmix64(seed, n) >> 40)",
                             "(oracle_splitmix64(seed, n) >> 41)"),
+    "topk_ties_to_highest_index": ("(best < 0 || zr[j] > zr[best])",
+                                   "(best < 0 || zr[j] >= zr[best])"),
+    "topk_unnormalised_logprob": ("logprob[r * K + q] = zr[best] - l;",
+                                  "logprob[r * K + q] = zr[best];"),
 }
 
 

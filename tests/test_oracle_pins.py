@@ -310,3 +310,55 @@ def test_payload_closed_form_against_pages():
         assert abs(red - (1.0 - 2.0 / V)) < 1e-15
         assert red > g["min_traffic_reduction"]
     assert round(g["r0_bytes_per_step"] / g["p0_bytes_per_step"]) == g["p0_ratio"]
+
+
+# ---------------------------------------------------------------- top-K log-prob surface
+@pytest.mark.parametrize("K", [1, 3, 7])
+def test_topk_bruteforce_on_exact_logits(K):
+    """Top-K ids and log-probs against a brute-force sort of exact rational logits by
+    (value descending, column ascending). Catches a wrong tie direction, an off-by-one in
+    the selection or a log-prob relative to the wrong normaliser."""
+    M, d, V = 4, 16, 40
+    Hb, Wb = _tiny(M, d, V, seed=17)
+    out = oracle.topk(Hb, Wb, K)
+    Ze = _exact_logits(Hb, Wb)
+    for r in range(M):
+        order = sorted(range(V), key=lambda j: (-Ze[r][j], j))[:K]
+        assert list(out["ids"][r]) == order
+        lse = _softmax_stats([float(v) for v in Ze[r]])
+        assert abs(out["lse"][r] - lse) < 1e-12
+        for q, j in enumerate(order):
+            assert abs(out["logprob"][r, q] - (float(Ze[r][j]) - lse)) < 1e-12
+
+
+def test_topk_ties_and_equal_logits():
+    """All-equal logits (H = 0) give ids 0..K-1 and log-prob -log V each; duplicated W rows
+    give equal logits listed by ascending column."""
+    V, d, K = 50, 8, 5
+    Hb = np.zeros((1, d), np.uint16)
+    _, Wb = _tiny(1, d, V, seed=1)
+    out = oracle.topk(Hb, Wb, K)
+    assert list(out["ids"][0]) == [0, 1, 2, 3, 4]
+    assert np.allclose(out["logprob"][0], -math.log(V), atol=1e-14)
+    H, W = synth.make_hw(1, 32, 64, seed=2)
+    W = W.clone()
+    W[30] = (H[0].float() * 5.0 / 32).to(torch.bfloat16)
+    W = synth.duplicate_rows(W, [(30, 3), (30, 63)])
+    out = oracle.topk(synth.bf16_bits(H), synth.bf16_bits(W), 4)
+    assert list(out["ids"][0][:3]) == [3, 30, 63]
+
+
+def test_topk_matches_numpy_stable_argsort():
+    """Against numpy's stable argsort of -z (a library routine) on a mid-size case, and the
+    K = 1 entry against the deterministic token surface."""
+    M, d, V, K = 6, 64, 3000, 16
+    Hb, Wb = _tiny(M, d, V, seed=23)
+    out = oracle.topk(Hb, Wb, K)
+    Z = oracle.logits(Hb, Wb)
+    ref = np.argsort(-Z, axis=1, kind="stable")[:, :K]
+    assert np.array_equal(out["ids"], ref)
+    proj = oracle.project(Hb, Wb, 3)
+    assert np.array_equal(out["ids"][:, 0], proj["token"])
+    assert np.allclose(out["logprob"][:, 0], proj["logprob"], atol=1e-13)
+    with pytest.raises(ValueError):
+        oracle.topk(Hb, Wb, V + 1)
