@@ -48,6 +48,8 @@ WORKLOADS = {
                      desc="seeded sampling: H[256,5120] x W[151936,5120] bf16, k=4, GUMBEL_TOKEN T=0.7"),
     "tiny": dict(M=4, d=256, V=4096, k=2, surface="token_logprob",
                  desc="tiny: H[4,256] x W[4096,256] bf16, k=2"),
+    "decode16_topk": dict(M=16, d=5120, V=151936, k=4, surface="topk_logprob", topk=8,
+                          desc="decode top-8 log-probs: H[16,5120] x W[151936,5120] bf16, k=4"),
     "sampling_token": dict(M=256, d=5120, V=151936, k=4, surface="token_logprob",
                            desc="256-row decode batch: H[256,5120] x W[151936,5120] bf16, k=4, TOKEN + log-prob"),
     # smaller cases of the same kernels for ncu captures (inputs still larger than L2)
@@ -280,7 +282,7 @@ def main():
     if rank:
         H = synth.make_hw(M, d, 1, seed=rank_rows_seed(rank), device="cuda")[0]
     targets = synth.make_targets(M, V, seed=1, device="cuda") if cfg.get("targets") else None
-    out, bufs = sb.make_outputs(M, V, k, surface, targets=targets)
+    out, bufs = sb.make_outputs(M, V, k, surface, targets=targets, topk=cfg.get("topk", 0))
     Tps = sb.sb_tiles_per_shard(M, V, k)
     stream = torch.cuda.current_stream()
 

@@ -14,9 +14,11 @@ import ctypes
 import os
 import threading
 
-SB_TOKEN, SB_TOKEN_LOGPROB, SB_FULL_LOGITS, SB_GUMBEL_TOKEN = 0, 1, 2, 3
+SB_TOKEN, SB_TOKEN_LOGPROB, SB_FULL_LOGITS, SB_GUMBEL_TOKEN, SB_TOPK_LOGPROB = 0, 1, 2, 3, 4
+SB_MAX_TOPK = 16
 SURFACES = {"token": SB_TOKEN, "token_logprob": SB_TOKEN_LOGPROB,
-            "full_logits": SB_FULL_LOGITS, "gumbel_token": SB_GUMBEL_TOKEN}
+            "full_logits": SB_FULL_LOGITS, "gumbel_token": SB_GUMBEL_TOKEN,
+            "topk_logprob": SB_TOPK_LOGPROB}
 SB_OK = 0
 SB_ERR_INVALID_ARG = 1
 SB_ERR_UNSUPPORTED = 2
@@ -41,7 +43,9 @@ class sb_outputs(ctypes.Structure):
     _fields_ = [("token", ctypes.c_void_p), ("token_logprob", ctypes.c_void_p),
                 ("lse", ctypes.c_void_p), ("logits_bf16", ctypes.c_void_p),
                 ("target_ids", ctypes.c_void_p), ("target_logprob", ctypes.c_void_p),
-                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("topk_ids", ctypes.c_void_p), ("topk_logprob", ctypes.c_void_p),
+                ("topk", ctypes.c_int32)]
 
 
 def lib():
@@ -165,7 +169,7 @@ def sb_debug_configure(stall_epilogue: bool, wait_limit_ns: int) -> int:
 
 # ------------------------------------------------------------------ convenience wrapper
 def make_outputs(M: int, V: int, k: int, surface: int, *, device="cuda", lse=True,
-                 logprob=True, targets=None, workspace=None):
+                 logprob=True, targets=None, workspace=None, topk: int = 0):
     """Allocate the caller-owned buffers of one call with torch; returns (sb_outputs, dict)."""
     import torch
     bufs = {"token": torch.empty(M, dtype=torch.int32, device=device)}
@@ -178,6 +182,9 @@ def make_outputs(M: int, V: int, k: int, surface: int, *, device="cuda", lse=Tru
     if targets is not None:
         bufs["target_ids"] = targets
         bufs["target_logprob"] = torch.empty(M, dtype=torch.float32, device=device)
+    if surface == SB_TOPK_LOGPROB:
+        bufs["topk_ids"] = torch.empty(M, topk, dtype=torch.int32, device=device)
+        bufs["topk_logprob"] = torch.empty(M, topk, dtype=torch.float32, device=device)
     nbytes = sb_workspace_bytes(M, V, k, surface)
     if nbytes == 0:
         raise SbError(SB_ERR_INVALID_ARG, "sb_workspace_bytes")
@@ -187,12 +194,14 @@ def make_outputs(M: int, V: int, k: int, surface: int, *, device="cuda", lse=Tru
     out = sb_outputs(_ptr(bufs["token"]), _ptr(bufs.get("token_logprob")), _ptr(bufs.get("lse")),
                      _ptr(bufs.get("logits")), _ptr(bufs.get("target_ids")),
                      _ptr(bufs.get("target_logprob")), _ptr(workspace),
-                     workspace.numel() * workspace.element_size())
+                     workspace.numel() * workspace.element_size(),
+                     _ptr(bufs.get("topk_ids")), _ptr(bufs.get("topk_logprob")), int(topk))
     return out, bufs
 
 
 def project(H, W, k: int, surface: int = SB_TOKEN_LOGPROB, *, temperature: float = 1.0,
-            seed: int = 0, targets=None, stream=None, lse=True, logprob=True, workspace=None):
+            seed: int = 0, targets=None, stream=None, lse=True, logprob=True, workspace=None,
+            topk: int = 0):
     """Run one projection call on torch CUDA tensors H [M, d] and W [V, d] (bf16).
 
     Returns the dict of output tensors (token, token_logprob, lse, logits, target_logprob,
@@ -200,7 +209,7 @@ def project(H, W, k: int, surface: int = SB_TOKEN_LOGPROB, *, temperature: float
     M, d = H.shape
     V = W.shape[0]
     out, bufs = make_outputs(M, V, k, surface, device=H.device, lse=lse, logprob=logprob,
-                             targets=targets, workspace=workspace)
+                             targets=targets, workspace=workspace, topk=topk)
     st = sb_lmhead_project(H, W, M, d, V, k, surface, temperature, seed, out, stream)
     if st != SB_OK:
         raise SbError(st, "sb_lmhead_project")

@@ -144,6 +144,130 @@ __global__ void __launch_bounds__(32 * kMaxWarps) combine_kernel(const CombinePa
     }
 }
 
+// Top-K: per (row, shard) warp, lane l keeps a sorted list (largest first, equal values by
+// ascending column) of the kMaxTopK best entries of its tiles l, l+32, ... (tiles, and the
+// entries within a tile, arrive in ascending column order, so an equal value already kept
+// has the lower column); then K rounds of a warp-wide max over the lanes' list heads give
+// the shard's top K.  Thread 0 merges the k shard lists the same way.  Selection compares
+// values only, so the result is the same for any order of these steps.
+__device__ __forceinline__ uint32_t ord_f(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float unord_f(uint32_t o) {
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+
+__global__ void __launch_bounds__(32 * kMaxWarps) combine_topk_kernel(const CombineParams p) {
+    extern __shared__ float sh[];  // k x (m, i, s), then k x K values, k x K columns
+    float *sm = sh;
+    int *si = reinterpret_cast<int *>(sh + p.k);
+    float *ss = sh + 2 * p.k;
+    const int K = p.topk;
+    float *slv = sh + 3 * p.k;
+    int *sli = reinterpret_cast<int *>(slv + p.k * K);
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int row = blockIdx.x;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int sh_i = warp; sh_i < p.k; sh_i += nwarps) {
+        Rec r{-INFINITY, INT_MAX, 0.f};
+        float tv[kMaxTopK];
+        int ti[kMaxTopK];
+#pragma unroll
+        for (int q = 0; q < kMaxTopK; ++q) {
+            tv[q] = -INFINITY;
+            ti[q] = INT_MAX;
+        }
+        const size_t base = (static_cast<size_t>(row) * p.k + sh_i) * p.T;
+        for (int t = lane; t < p.T; t += 32) {
+            r = merge(r, Rec{__ldg(p.ws.m + base + t), __ldg(p.ws.idx + base + t),
+                             __ldg(p.ws.s + base + t)});
+            const size_t o = (base + t) * K;
+            for (int e = 0; e < K; ++e) {
+                const float x = __ldg(p.ws.tkv + o + e);
+                if (!(x > tv[kMaxTopK - 1])) break;  // entries are sorted: the rest lose too
+                float cv = x;
+                int ci = __ldg(p.ws.tki + o + e);
+                bool ins = false;
+#pragma unroll
+                for (int q = 0; q < kMaxTopK; ++q) {
+                    if (ins || cv > tv[q]) {
+                        const float a = tv[q];
+                        const int b = ti[q];
+                        tv[q] = cv;
+                        ti[q] = ci;
+                        cv = a;
+                        ci = b;
+                        ins = true;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const Rec o{__shfl_xor_sync(0xFFFFFFFFu, r.m, off),
+                        __shfl_xor_sync(0xFFFFFFFFu, r.i, off),
+                        __shfl_xor_sync(0xFFFFFFFFu, r.s, off)};
+            r = merge(r, o);
+        }
+        int hp = 0;  // this lane's list head
+        for (int q = 0; q < K; ++q) {
+            float hv = -INFINITY;
+            int hi = INT_MAX;
+#pragma unroll
+            for (int e = 0; e < kMaxTopK; ++e)
+                if (e == hp) {
+                    hv = tv[e];
+                    hi = ti[e];
+                }
+            const uint32_t om = __reduce_max_sync(0xFFFFFFFFu, ord_f(hv));
+            const int wi = __reduce_min_sync(0xFFFFFFFFu, ord_f(hv) == om ? hi : INT_MAX);
+            if (hi == wi && ord_f(hv) == om && hp < kMaxTopK) ++hp;
+            if (lane == 0) {
+                slv[sh_i * K + q] = unord_f(om);
+                sli[sh_i * K + q] = wi;
+            }
+        }
+        if (lane == 0) {
+            sm[sh_i] = r.m;
+            si[sh_i] = r.i;
+            ss[sh_i] = r.s;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    Rec acc{-INFINITY, INT_MAX, 0.f};
+    for (int s2 = 0; s2 < p.k; ++s2) acc = merge(acc, Rec{sm[s2], si[s2], ss[s2]});
+    const float lse = acc.m + logf(acc.s);
+    p.token[row] = acc.i;
+    if (p.lse) p.lse[row] = lse;
+    if (p.token_logprob) p.token_logprob[row] = -logf(acc.s);
+    if (p.target_logprob) p.target_logprob[row] = p.ws.tz[row] - lse;
+    // k-way merge of the sorted shard lists; the heads are kept in the first k ints of the
+    // shard (m) array, no longer needed
+    int *heads = reinterpret_cast<int *>(sm);
+    for (int s2 = 0; s2 < p.k; ++s2) heads[s2] = 0;
+    for (int q = 0; q < K; ++q) {
+        float bv = -INFINITY;
+        int bi = INT_MAX, bs = -1;
+        for (int s2 = 0; s2 < p.k; ++s2) {
+            if (heads[s2] >= K) continue;
+            const float v = slv[s2 * K + heads[s2]];
+            const int i = sli[s2 * K + heads[s2]];
+            if (v > bv || (v == bv && i < bi)) {
+                bv = v;
+                bi = i;
+                bs = s2;
+            }
+        }
+        if (bs >= 0) ++heads[bs];
+        p.topk_ids[static_cast<size_t>(row) * K + q] = bi;
+        p.topk_logprob[static_cast<size_t>(row) * K + q] = bv - lse;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
@@ -158,6 +282,10 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (p.flags & kFlagTopk) {
+        cfg.dynamicSmemBytes = static_cast<size_t>(p.k) * (12 + 8 * p.topk);
+        return cudaLaunchKernelEx(&cfg, combine_topk_kernel, p);
+    }
     if (p.flags & kFlagGumbel) return cudaLaunchKernelEx(&cfg, combine_kernel<true>, p);
     return cudaLaunchKernelEx(&cfg, combine_kernel<false>, p);
 }

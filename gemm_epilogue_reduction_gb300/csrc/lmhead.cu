@@ -73,6 +73,7 @@ __host__ __device__ inline SmemLayout make_layout(int nb, int stages_a, int stag
     off += vocab ? kMaxVocabModeRows * 4 : 0;
     L.scratch_off = off;
     off += vocab ? 4 * nb * ((flags & kFlagGumbel) ? 24 : 12) : 0;
+    off += (vocab && (flags & kFlagTopk)) ? 4 * nb * kMaxTopK * 8 : 0;
     L.total = off + 1024;  // slack to align the base to 1024 bytes
     return L;
 }
@@ -173,12 +174,16 @@ __device__ __forceinline__ uint16_t bf16_bits_rn(float z) {
 // (TMEM columns).  The two warps of a quadrant take alternate 32-row chunks (half h takes
 // chunks h, h+2, ...).  Per row: warp max / lowest argmax / sum of exp with warp reductions,
 // then the four quadrants' partial records merge in quadrant order through shared memory.
-template <bool GUMBEL, bool FULL>
+template <int EPI>
 __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCoord &c,
                                                uint32_t taddr, uint64_t *tempty_b, int q,
                                                int h, int lane, const int32_t *tgt_s,
                                                float *scratch) {
+    constexpr bool GUMBEL = EPI == kEpiGumbel;
+    constexpr bool FULL = EPI == kEpiFull;
+    constexpr bool TOPK = EPI == kEpiTopk;
     const int nb = p.nb;
+    const int K = p.topk;
     const int v = c.v0 + 32 * q + lane;
     const bool valid = v < c.v_end;
     const bool has_t = (p.flags & kFlagTargets) != 0;
@@ -188,6 +193,9 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
     float *sc_gk = scratch + 12 * nb;
     int *sc_gi = reinterpret_cast<int *>(scratch + 16 * nb);
     float *sc_gz = scratch + 20 * nb;
+    // top-K scratch: [quadrant][row][kMaxTopK] values, then the same for columns
+    float *sc_tv = scratch + 12 * nb;
+    int *sc_ti = reinterpret_cast<int *>(sc_tv + 4 * nb * kMaxTopK);
 
     for (int c0 = 32 * h; c0 < nb; c0 += 64) {
         uint32_t raw[32];
@@ -198,6 +206,8 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
             tmem_ld32x32b_x16(taddr + c0, raw);
         float my_m = -INFINITY, my_s = 0.f, my_gk = -INFINITY, my_gz = 0.f;
         int my_i = INT_MAX, my_gi = INT_MAX;
+        float my_tv[TOPK ? kMaxTopK : 1];
+        int my_ti[TOPK ? kMaxTopK : 1];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             const int row = c0 + j;
@@ -227,6 +237,23 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
                     my_gz = gz;
                 }
             }
+            if (TOPK) {
+                // the quadrant's K largest of this row: K rounds of warp max (lowest column
+                // on ties), each removing its winner
+                bool alive = valid;
+#pragma unroll
+                for (int r = 0; r < kMaxTopK; ++r) {
+                    if (r >= K) break;
+                    const uint32_t oc = alive ? oy : float_to_ordered(-INFINITY);
+                    const uint32_t ocm = __reduce_max_sync(0xFFFFFFFFu, oc);
+                    const int ci = __reduce_min_sync(0xFFFFFFFFu, (alive && oc == ocm) ? v : INT_MAX);
+                    if (v == ci) alive = false;
+                    if (lane == j) {
+                        my_tv[r] = ordered_to_float(ocm);
+                        my_ti[r] = ci;
+                    }
+                }
+            }
             if (FULL && valid) p.logits[static_cast<size_t>(row) * p.V + v] = bf16_bits_rn(z);
             if (has_t && valid && tgt_s[row] == v) p.ws.tz[row] = z;
             if (lane == j) {
@@ -244,6 +271,14 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
                 sc_gk[o] = my_gk;
                 sc_gi[o] = my_gi;
                 sc_gz[o] = my_gz;
+            }
+            if (TOPK) {
+#pragma unroll
+                for (int r = 0; r < kMaxTopK; ++r) {
+                    if (r >= K) break;
+                    sc_tv[o * kMaxTopK + r] = my_tv[r];
+                    sc_ti[o * kMaxTopK + r] = my_ti[r];
+                }
             }
         }
     }
@@ -289,6 +324,32 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
             p.ws.gi[ri] = gi;
             p.ws.gz[ri] = gz;
         }
+        if (TOPK) {  // merge the four quadrants' sorted lists into the tile's top K
+            int p0 = 0, p1 = 0, p2 = 0, p3 = 0;
+            for (int r = 0; r < K; ++r) {
+                float bv = -INFINITY;
+                int bi = INT_MAX, bw = -1;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const int pw = w == 0 ? p0 : (w == 1 ? p1 : (w == 2 ? p2 : p3));
+                    if (pw >= K) continue;
+                    const int o = (w * nb + row) * kMaxTopK + pw;
+                    const float vw = sc_tv[o];
+                    const int iw = sc_ti[o];
+                    if (vw > bv || (vw == bv && iw < bi)) {
+                        bv = vw;
+                        bi = iw;
+                        bw = w;
+                    }
+                }
+                p0 += bw == 0;
+                p1 += bw == 1;
+                p2 += bw == 2;
+                p3 += bw == 3;
+                p.ws.tkv[ri * K + r] = bv;
+                p.ws.tki[ri * K + r] = bi;
+            }
+        }
     }
     epi_bar_sync();
 }
@@ -298,10 +359,13 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
 // [v0 + 128h, v0 + 128h + 128) of the 256-column tile, i.e. record tile 2t + h.  It walks
 // them in chunks of 32: chunk max and first argmax, online rescale of the running sum, then
 // the sum of exp against the running max.
-template <bool GUMBEL, bool FULL>
+template <int EPI>
 __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoord &c,
                                               uint32_t taddr, uint64_t *tempty_b, int q, int h,
                                               int lane) {
+    constexpr bool GUMBEL = EPI == kEpiGumbel;
+    constexpr bool FULL = EPI == kEpiFull;
+    constexpr bool TOPK = EPI == kEpiTopk;
     const int row = c.m0 + 32 * q + lane;
     const bool rv = row < p.M;
     const int rt = 2 * c.t + h;                 // record tile within the shard
@@ -309,6 +373,17 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
     const int tgt = ((p.flags & kFlagTargets) && rv) ? __ldg(p.targets + row) : -1;
     float rm = -INFINITY, rs = 0.f, gk = -INFINITY, gz = 0.f;
     int ri = INT_MAX, gi = INT_MAX;
+    // top-K: a sorted list (largest first, equal values by ascending column) of the
+    // kMaxTopK largest seen; only the first K are written
+    float tv[TOPK ? kMaxTopK : 1];
+    int ti[TOPK ? kMaxTopK : 1];
+    if (TOPK) {
+#pragma unroll
+        for (int r = 0; r < kMaxTopK; ++r) {
+            tv[r] = -INFINITY;
+            ti[r] = INT_MAX;
+        }
+    }
     constexpr int kChunks = kRecordCols / 32;
 #pragma unroll 1
     for (int ch = 0; ch < kChunks; ++ch) {
@@ -358,6 +433,31 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
                 }
             }
         }
+        if (TOPK) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                if (y[j] > tv[kMaxTopK - 1]) {  // invalid columns are -inf: never inserted
+                    // columns arrive in ascending order, so an equal value already in the
+                    // list has a lower column and stays ahead; after the insertion point
+                    // every entry shifts down by one
+                    float cv = y[j];
+                    int ci = cb + j;
+                    bool ins = false;
+#pragma unroll
+                    for (int r = 0; r < kMaxTopK; ++r) {
+                        if (ins || cv > tv[r]) {
+                            const float tvr = tv[r];
+                            const int tir = ti[r];
+                            tv[r] = cv;
+                            ti[r] = ci;
+                            cv = tvr;
+                            ci = tir;
+                            ins = true;
+                        }
+                    }
+                }
+            }
+        }
         if (tgt >= cb && tgt < cb + nval) {
             float tzv = 0.f;
 #pragma unroll
@@ -394,6 +494,14 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
             p.ws.gk[o] = gk;
             p.ws.gi[o] = gi;
             p.ws.gz[o] = gz;
+        }
+        if (TOPK) {
+#pragma unroll
+            for (int r = 0; r < kMaxTopK; ++r) {
+                if (r >= p.topk) break;
+                p.ws.tkv[o * p.topk + r] = tv[r];
+                p.ws.tki[o * p.topk + r] = ti[r];
+            }
         }
     }
 }
@@ -447,7 +555,7 @@ __device__ TileCoord coord_fn(const GemmParams &p, int tile, int rank) {
     return tile_coord<VOCAB, CS>(p, tile, rank);
 }
 
-template <bool VOCAB, bool GUMBEL, bool FULL, int CS>
+template <bool VOCAB, int EPI, int CS>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const GemmParams p, const uint32_t tmem_cols) {
@@ -603,9 +711,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * p.nb);
             if (VOCAB)
-                epilogue_vocab<GUMBEL, FULL>(p, c, taddr, &tempty[b], q, h, lane, tgt_s, scratch);
+                epilogue_vocab<EPI>(p, c, taddr, &tempty[b], q, h, lane, tgt_s, scratch);
             else
-                epilogue_rows<GUMBEL, FULL>(p, c, taddr, &tempty[b], q, h, lane);
+                epilogue_rows<EPI>(p, c, taddr, &tempty[b], q, h, lane);
         }
     }
 
@@ -621,10 +729,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool VOCAB, bool GUMBEL, bool FULL, int CS>
+template <bool VOCAB, int EPI, int CS>
 cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p,
                      size_t smem, int num_sms, cudaStream_t stream) {
-    auto kern = lmhead_kernel<VOCAB, GUMBEL, FULL, CS>;
+    auto kern = lmhead_kernel<VOCAB, EPI, CS>;
     // The shared-memory opt-in is per device; every launch asks for at most kSmemLimit.
     static std::atomic<uint64_t> opted_in{0};
     int dev = 0;
@@ -683,19 +791,25 @@ size_t lmhead_smem_bytes(int nb, int stages_a, int stages_b, bool vocab_mode, in
 
 cudaError_t launch_lmhead(bool vocab_mode, const CUtensorMap &tmA, const CUtensorMap &tmB,
                           const GemmParams &p, size_t smem, int num_sms, cudaStream_t stream) {
-    const bool g = (p.flags & kFlagGumbel) != 0;
-    const bool f = (p.flags & kFlagFull) != 0;
-    if (vocab_mode) {
-        if (g) return f ? launch_t<true, true, true, 1>(tmA, tmB, p, smem, num_sms, stream)
-                        : launch_t<true, true, false, 1>(tmA, tmB, p, smem, num_sms, stream);
-        return f ? launch_t<true, false, true, 1>(tmA, tmB, p, smem, num_sms, stream)
-                 : launch_t<true, false, false, 1>(tmA, tmB, p, smem, num_sms, stream);
-    }
+    const int epi = (p.flags & kFlagGumbel) ? kEpiGumbel
+                    : (p.flags & kFlagFull) ? kEpiFull
+                    : (p.flags & kFlagTopk) ? kEpiTopk
+                                            : kEpiPlain;
     constexpr int C = kRowsCluster;
-    if (g) return f ? launch_t<false, true, true, C>(tmA, tmB, p, smem, num_sms, stream)
-                    : launch_t<false, true, false, C>(tmA, tmB, p, smem, num_sms, stream);
-    return f ? launch_t<false, false, true, C>(tmA, tmB, p, smem, num_sms, stream)
-             : launch_t<false, false, false, C>(tmA, tmB, p, smem, num_sms, stream);
+    switch (epi) {
+    case kEpiGumbel:
+        return vocab_mode ? launch_t<true, kEpiGumbel, 1>(tmA, tmB, p, smem, num_sms, stream)
+                          : launch_t<false, kEpiGumbel, C>(tmA, tmB, p, smem, num_sms, stream);
+    case kEpiFull:
+        return vocab_mode ? launch_t<true, kEpiFull, 1>(tmA, tmB, p, smem, num_sms, stream)
+                          : launch_t<false, kEpiFull, C>(tmA, tmB, p, smem, num_sms, stream);
+    case kEpiTopk:
+        return vocab_mode ? launch_t<true, kEpiTopk, 1>(tmA, tmB, p, smem, num_sms, stream)
+                          : launch_t<false, kEpiTopk, C>(tmA, tmB, p, smem, num_sms, stream);
+    default:
+        return vocab_mode ? launch_t<true, kEpiPlain, 1>(tmA, tmB, p, smem, num_sms, stream)
+                          : launch_t<false, kEpiPlain, C>(tmA, tmB, p, smem, num_sms, stream);
+    }
 }
 
 }  // namespace sb

@@ -25,10 +25,10 @@ size_t al256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 struct WsLayout {
-    size_t m, idx, s, gk, gi, gz, tz, total;
+    size_t m, idx, s, gk, gi, gz, tkv, tki, tz, total;
 };
 
-WsLayout ws_layout(int64_t M, int32_t k, int32_t T, bool gumbel) {
+WsLayout ws_layout(int64_t M, int32_t k, int32_t T, bool gumbel, int topk = 0) {
     const size_t n = static_cast<size_t>(M) * k * T;
     WsLayout L{};
     size_t off = 256;
@@ -46,13 +46,19 @@ WsLayout ws_layout(int64_t M, int32_t k, int32_t T, bool gumbel) {
         L.gz = off;
         off += al256(4 * n);
     }
+    if (topk > 0) {
+        L.tkv = off;
+        off += al256(4 * n * topk);
+        L.tki = off;
+        off += al256(4 * n * topk);
+    }
     L.tz = off;
     off += al256(4 * static_cast<size_t>(M));
     L.total = off;
     return L;
 }
 
-Workspace ws_views(void *base, const WsLayout &L, bool gumbel) {
+Workspace ws_views(void *base, const WsLayout &L, bool gumbel, int topk = 0) {
     uint8_t *b = static_cast<uint8_t *>(base);
     Workspace w{};
     w.epoch = reinterpret_cast<uint32_t *>(b);
@@ -64,6 +70,10 @@ Workspace ws_views(void *base, const WsLayout &L, bool gumbel) {
         w.gk = reinterpret_cast<float *>(b + L.gk);
         w.gi = reinterpret_cast<int32_t *>(b + L.gi);
         w.gz = reinterpret_cast<float *>(b + L.gz);
+    }
+    if (topk > 0) {
+        w.tkv = reinterpret_cast<float *>(b + L.tkv);
+        w.tki = reinterpret_cast<int32_t *>(b + L.tki);
     }
     w.tz = reinterpret_cast<float *>(b + L.tz);
     return w;
@@ -166,6 +176,9 @@ int32_t current_device(DevInfo *out) {
 
 int32_t check_outputs(const sb_outputs *out, int32_t surface, bool need_ws) {
     if (!out || !out->token) return SB_ERR_INVALID_ARG;
+    if (surface == SB_TOPK_LOGPROB &&
+        (!out->topk_ids || !out->topk_logprob || out->topk < 1 || out->topk > kMaxTopK))
+        return SB_ERR_INVALID_ARG;
     if ((surface == SB_TOKEN_LOGPROB || surface == SB_GUMBEL_TOKEN) && !out->token_logprob)
         return SB_ERR_INVALID_ARG;
     if (surface == SB_FULL_LOGITS && !out->logits_bf16) return SB_ERR_INVALID_ARG;
@@ -173,7 +186,9 @@ int32_t check_outputs(const sb_outputs *out, int32_t surface, bool need_ws) {
     if (need_ws && !out->workspace) return SB_ERR_INVALID_ARG;
     if (!aligned(out->token, 4) || !aligned(out->token_logprob, 4) || !aligned(out->lse, 4) ||
         !aligned(out->target_ids, 4) || !aligned(out->target_logprob, 4) ||
-        !aligned(out->logits_bf16, 16) || !aligned(out->workspace, 256))
+        !aligned(out->logits_bf16, 16) || !aligned(out->workspace, 256) ||
+        (surface == SB_TOPK_LOGPROB &&
+         (!aligned(out->topk_ids, 4) || !aligned(out->topk_logprob, 4))))
         return SB_ERR_ALIGNMENT;
     return SB_OK;
 }
@@ -214,6 +229,11 @@ CombineParams combine_params(const sb_outputs *out, const Workspace &w, int64_t 
     c.token_logprob = out->token_logprob;
     c.lse = out->lse;
     c.target_logprob = out->target_ids ? out->target_logprob : nullptr;
+    if (flags & kFlagTopk) {
+        c.topk = out->topk;
+        c.topk_ids = out->topk_ids;
+        c.topk_logprob = out->topk_logprob;
+    }
     return c;
 }
 
@@ -222,8 +242,10 @@ CombineParams combine_params(const sb_outputs *out, const Workspace &w, int64_t 
 extern "C" {
 
 size_t sb_workspace_bytes(int64_t M, int64_t V, int32_t k, int32_t surface) {
-    if (!shape_ok(M, V, k) || surface < SB_TOKEN || surface > SB_GUMBEL_TOKEN) return 0;
-    return ws_layout(M, k, tiles_per_shard(M, V, k), surface == SB_GUMBEL_TOKEN).total;
+    if (!shape_ok(M, V, k) || surface < SB_TOKEN || surface > SB_TOPK_LOGPROB) return 0;
+    return ws_layout(M, k, tiles_per_shard(M, V, k), surface == SB_GUMBEL_TOKEN,
+                     surface == SB_TOPK_LOGPROB ? kMaxTopK : 0)
+        .total;
 }
 
 int32_t sb_tiles_per_shard(int64_t M, int64_t V, int32_t k) {
@@ -241,21 +263,24 @@ int32_t enqueue(const void *H, const void *W, int64_t M, int64_t d, int64_t V, i
                 int32_t surface, float temperature, uint64_t seed, const sb_outputs *out,
                 void *stream, bool with_combine) {
     if (!H || !W || !shape_ok(M, V, k) || d < 8 || d > (int64_t(1) << 24) ||
-        surface < SB_TOKEN || surface > SB_GUMBEL_TOKEN)
+        surface < SB_TOKEN || surface > SB_TOPK_LOGPROB)
         return SB_ERR_INVALID_ARG;
     const bool gumbel = surface == SB_GUMBEL_TOKEN;
+    const bool topk = surface == SB_TOPK_LOGPROB;
     if (gumbel && !(std::isfinite(temperature) && temperature > 0.f)) return SB_ERR_INVALID_ARG;
     if (int32_t e = check_outputs(out, surface, true)) return e;
+    if (topk && (out->topk > V || k > kMaxTopKShards)) return SB_ERR_INVALID_ARG;
     if (d % 8 != 0 || !aligned(H, 16) || !aligned(W, 16)) return SB_ERR_ALIGNMENT;
     const int32_t T = tiles_per_shard(M, V, k);
-    const WsLayout L = ws_layout(M, k, T, gumbel);
+    const int K = topk ? out->topk : 0;
+    const WsLayout L = ws_layout(M, k, T, gumbel, K);
     if (out->workspace_bytes < L.total) return SB_ERR_WORKSPACE_TOO_SMALL;
     DevInfo dev;
     if (int32_t e = current_device(&dev)) return e;
 
     const bool vm = vocab_mode(M);
     const int flags = (gumbel ? kFlagGumbel : 0) | (surface == SB_FULL_LOGITS ? kFlagFull : 0) |
-                      (out->target_ids ? kFlagTargets : 0);
+                      (out->target_ids ? kFlagTargets : 0) | (topk ? kFlagTopk : 0);
     const float inv_t = gumbel ? 1.0f / temperature : 1.0f;
     GemmParams p{};
     p.M = static_cast<int>(M);
@@ -276,11 +301,12 @@ int32_t enqueue(const void *H, const void *W, int64_t M, int64_t d, int64_t V, i
     p.kblocks = static_cast<int>((d + kBlockK - 1) / kBlockK);
     if (!pick_stages(p.nb, vm, p.m_tiles, flags, &p.stages_a, &p.stages_b)) return SB_ERR_UNSUPPORTED;
     p.flags = flags;
+    p.topk = K;
     p.inv_t = inv_t;
     p.seed = seed;
     p.targets = out->target_ids;
     p.logits = out->logits_bf16;
-    p.ws = ws_views(out->workspace, L, gumbel);
+    p.ws = ws_views(out->workspace, L, gumbel, K);
     p.epoch = g_epoch.fetch_add(1) + 1;
     p.timeout_ns = g_timeout_ns.load();
     p.debug_stall = g_debug_stall.load();
@@ -321,19 +347,23 @@ int32_t sb_combine_shard_records(const void *workspace, int64_t M, int32_t k,
                                  const sb_outputs *out, void *stream) {
     if (!workspace || M < 1 || M > (int64_t(1) << 30) || k < 1 || k > kMaxShards ||
         tiles_per_shard_ < 1 ||
-        surface < SB_TOKEN || surface > SB_GUMBEL_TOKEN)
+        surface < SB_TOKEN || surface > SB_TOPK_LOGPROB)
         return SB_ERR_INVALID_ARG;
     const bool gumbel = surface == SB_GUMBEL_TOKEN;
+    const bool topk = surface == SB_TOPK_LOGPROB;
+    if (topk && k > kMaxTopKShards) return SB_ERR_INVALID_ARG;
     if (gumbel && !(std::isfinite(temperature) && temperature > 0.f)) return SB_ERR_INVALID_ARG;
     if (int32_t e = check_outputs(out, surface == SB_FULL_LOGITS ? SB_TOKEN : surface, true))
         return e;
     if (out->workspace != workspace) return SB_ERR_INVALID_ARG;
-    const WsLayout L = ws_layout(M, k, tiles_per_shard_, gumbel);
+    const int K = topk ? out->topk : 0;
+    const WsLayout L = ws_layout(M, k, tiles_per_shard_, gumbel, K);
     if (out->workspace_bytes < L.total) return SB_ERR_WORKSPACE_TOO_SMALL;
     DevInfo dev;
     if (int32_t e = current_device(&dev)) return e;
-    const int flags = (gumbel ? kFlagGumbel : 0) | (out->target_ids ? kFlagTargets : 0);
-    const Workspace w = ws_views(const_cast<void *>(workspace), L, gumbel);
+    const int flags = (gumbel ? kFlagGumbel : 0) | (out->target_ids ? kFlagTargets : 0) |
+                      (topk ? kFlagTopk : 0);
+    const Workspace w = ws_views(const_cast<void *>(workspace), L, gumbel, K);
     const CombineParams c = combine_params(out, w, M, k, tiles_per_shard_, flags,
                                            gumbel ? 1.0f / temperature : 1.0f);
     if (launch_combine(c, static_cast<cudaStream_t>(stream)) != cudaSuccess) return SB_ERR_CUDA;

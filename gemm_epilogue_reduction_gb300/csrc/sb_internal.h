@@ -27,8 +27,13 @@ constexpr int kFirstEpiWarp = 3;     // warps 0 and 2 load, warp 1 issues MMAs +
 constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
 constexpr size_t kSmemLimit = 232448;  // 227 KB dynamic shared memory per CTA
 
+constexpr int kMaxTopK = 16;         // largest K of the top-K log-prob surface
+constexpr int kMaxTopKShards = 128;  // largest k with the top-K surface (combine smem)
+
 // Surface flags the kernels specialise on.
-enum : int { kFlagGumbel = 1, kFlagFull = 2, kFlagTargets = 4 };
+enum : int { kFlagGumbel = 1, kFlagFull = 2, kFlagTargets = 4, kFlagTopk = 8 };
+// Epilogue variants (one per surface family).
+enum : int { kEpiPlain = 0, kEpiFull = 1, kEpiGumbel = 2, kEpiTopk = 3 };
 
 struct Workspace {       // device views into the caller's workspace
     uint32_t *epoch;     // header word 0
@@ -39,6 +44,8 @@ struct Workspace {       // device views into the caller's workspace
     float *gk;
     int32_t *gi;
     float *gz;
+    float *tkv;          // [n][topk] top-K values per record (top-K surface)
+    int32_t *tki;        // [n][topk] their columns
     float *tz;
 };
 
@@ -55,6 +62,7 @@ struct GemmParams {
     int stages_a;          // ring depth of the UMMA A operand (16 KB stages)
     int stages_b;          // ring depth of the UMMA B operand (nb * 128 B stages)
     int flags;
+    int topk;              // K of the top-K surface (0 otherwise)
     float inv_t;
     unsigned long long seed;
     const int32_t *targets;
@@ -68,6 +76,9 @@ struct GemmParams {
 struct CombineParams {
     int M, k, T;
     int flags;
+    int topk;
+    int32_t *topk_ids;
+    float *topk_logprob;
     float inv_t;
     Workspace ws;
     int32_t *token;

@@ -47,8 +47,12 @@ typedef enum sb_surface {
     SB_TOKEN = 0,        /* deterministic argmax token (int32, lowest index on ties)      */
     SB_TOKEN_LOGPROB = 1,/* token + its natural-log log-probability over the full vocab   */
     SB_FULL_LOGITS = 2,  /* token + bf16 logits [M, V] in shard-to-full (global) layout    */
-    SB_GUMBEL_TOKEN = 3  /* counter-based Gumbel-max sample from softmax(z / T) + log-prob */
+    SB_GUMBEL_TOKEN = 3, /* counter-based Gumbel-max sample from softmax(z / T) + log-prob */
+    SB_TOPK_LOGPROB = 4  /* token + the K most likely tokens and their log-probabilities   */
 } sb_surface;
+
+/* Largest K of the SB_TOPK_LOGPROB surface. */
+#define SB_MAX_TOPK 16
 
 typedef enum sb_status {
     SB_OK = 0,
@@ -79,6 +83,11 @@ typedef enum sb_status {
  *                                  bytes, 256-byte aligned; holds the per-tile records, the
  *                                  target logits and the device status word.  Its contents
  *                                  need no initialisation.
+ *   topk_ids        int32 [M*K]    SB_TOPK_LOGPROB: per row the K columns with the largest
+ *                                  logits, largest first, equal logits by ascending column.
+ *   topk_logprob    float [M*K]    SB_TOPK_LOGPROB: their log-probabilities z_j - lse.
+ *   topk            K              SB_TOPK_LOGPROB: 1 <= K <= min(SB_MAX_TOPK, V); ignored by
+ *                                  the other surfaces (as are the two arrays above).
  */
 typedef struct sb_outputs {
     int32_t *token;
@@ -89,6 +98,9 @@ typedef struct sb_outputs {
     float *target_logprob;
     void *workspace;
     size_t workspace_bytes;
+    int32_t *topk_ids;
+    float *topk_logprob;
+    int32_t topk;
 } sb_outputs;
 
 /*
@@ -102,6 +114,8 @@ typedef struct sb_outputs {
  *   float   gkey[n]  SB_GUMBEL_TOKEN only: max of y + g over the tile
  *   int32   gidx[n]  SB_GUMBEL_TOKEN only: lowest column attaining gkey
  *   float   gz[n]    SB_GUMBEL_TOKEN only: z at gidx
+ *   float   tkv[n][K] SB_TOPK_LOGPROB only: the tile's K largest logits, largest first
+ *   int32   tki[n][K] SB_TOPK_LOGPROB only: their columns (INT32_MAX marks an empty slot)
  *   float   tz[M]    z at target_ids[r] (written only when targets are given)
  * Record (r, s, t) sits at index (r * k + s) * T + t and covers the global columns
  * [s*S + 128t, min(s*S + 128(t+1), (s+1)*S)) with S = V/k and T = ceil(S / 128).  y is z,
@@ -109,7 +123,8 @@ typedef struct sb_outputs {
  * noise of sb_lmhead_project.
  */
 
-/* Bytes of workspace one call needs; 0 if the arguments are invalid. */
+/* Bytes of workspace one call needs (for SB_TOPK_LOGPROB: with K = SB_MAX_TOPK, enough for
+ * every K); 0 if the arguments are invalid. */
 size_t sb_workspace_bytes(int64_t M, int64_t V, int32_t k, int32_t surface);
 
 /* Records per (row, lane shard): T = ceil((V / k) / 128), one per 128 vocabulary columns;

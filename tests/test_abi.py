@@ -55,6 +55,8 @@ def test_tiles_per_shard_and_workspace_layout():
     assert sb.sb_workspace_bytes(M, V, k, sb.SB_GUMBEL_TOKEN) == 256 + 6 * al(4 * n) + al(4 * M)
     assert sb.sb_workspace_bytes(0, V, k, sb.SB_TOKEN) == 0
     assert sb.sb_workspace_bytes(M, V, k, 7) == 0
+    assert sb.sb_workspace_bytes(M, V, k, sb.SB_TOPK_LOGPROB) == (
+        256 + 3 * al(4 * n) + 2 * al(4 * n * sb.SB_MAX_TOPK) + al(4 * M))
 
 
 def test_status_strings():
@@ -77,7 +79,6 @@ def _outputs(ws_bytes=1 << 20, **kw):
     (dict(M=0), sb.SB_ERR_INVALID_ARG),
     (dict(V=4097), sb.SB_ERR_INVALID_ARG),      # V % k != 0
     (dict(k=0), sb.SB_ERR_INVALID_ARG),
-    (dict(surface=4), sb.SB_ERR_INVALID_ARG),
     (dict(d=4), sb.SB_ERR_INVALID_ARG),
     (dict(d=260), sb.SB_ERR_ALIGNMENT),          # d % 8 != 0
     (dict(H=0x10000008), sb.SB_ERR_ALIGNMENT),
@@ -89,6 +90,14 @@ def _outputs(ws_bytes=1 << 20, **kw):
     (dict(out=dict(target_ids=0x20000000)), sb.SB_ERR_INVALID_ARG),  # no target_logprob
     (dict(out=dict(workspace=0x10000010)), sb.SB_ERR_ALIGNMENT),
     (dict(out=dict(workspace_bytes=1024)), sb.SB_ERR_WORKSPACE_TOO_SMALL),
+    (dict(surface=sb.SB_TOPK_LOGPROB), sb.SB_ERR_INVALID_ARG),  # no top-K buffers
+    (dict(surface=sb.SB_TOPK_LOGPROB,
+          out=dict(topk_ids=0x50000000, topk_logprob=0x60000000, topk=17)), sb.SB_ERR_INVALID_ARG),
+    (dict(surface=sb.SB_TOPK_LOGPROB, V=8, k=1,
+          out=dict(topk_ids=0x50000000, topk_logprob=0x60000000, topk=9)), sb.SB_ERR_INVALID_ARG),
+    (dict(surface=sb.SB_TOPK_LOGPROB, V=1024, k=256,
+          out=dict(topk_ids=0x50000000, topk_logprob=0x60000000, topk=4)), sb.SB_ERR_INVALID_ARG),
+    (dict(surface=5), sb.SB_ERR_INVALID_ARG),
 ])
 def test_invalid_arguments_are_rejected_before_any_launch(case, expect):
     args = dict(H=0x30000000, W=0x40000000, M=4, d=256, V=4096, k=2, surface=sb.SB_TOKEN,
