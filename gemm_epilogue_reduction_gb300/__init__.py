@@ -74,6 +74,13 @@ def lib():
         L.sb_combine_shard_records.argtypes = [P, i64, i32, i32, i32, ctypes.c_float,
                                                ctypes.POINTER(sb_outputs), P]
         L.sb_combine_shard_records.restype = i32
+        L.sb_payload_bytes.argtypes = [i64, i32, i32]
+        L.sb_payload_bytes.restype = ctypes.c_size_t
+        L.sb_pack_shard_records.argtypes = [P, i64, i32, i32, i32, i64, P, P]
+        L.sb_pack_shard_records.restype = i32
+        L.sb_merge_shard_payload.argtypes = [P, i64, i32, i32, ctypes.c_float,
+                                             ctypes.POINTER(sb_outputs), P]
+        L.sb_merge_shard_payload.restype = i32
         L.sb_last_device_status.argtypes = [ctypes.POINTER(sb_outputs)]
         L.sb_last_device_status.restype = i32
         L.sb_status_string.argtypes = [i32]
@@ -142,6 +149,22 @@ def sb_combine_shard_records(workspace, M, k, tiles_per_shard, surface, temperat
     return int(lib().sb_combine_shard_records(_ptr(workspace), M, k, tiles_per_shard,
                                               surface, float(temperature),
                                               ctypes.byref(out), _stream(stream)))
+
+
+def sb_payload_bytes(M: int, k: int, surface: int) -> int:
+    return int(lib().sb_payload_bytes(M, k, surface))
+
+
+def sb_pack_shard_records(workspace, M, k, tiles_per_shard, surface, col_offset, payload,
+                          stream=None) -> int:
+    return int(lib().sb_pack_shard_records(_ptr(workspace), M, k, tiles_per_shard, surface,
+                                           int(col_offset), _ptr(payload), _stream(stream)))
+
+
+def sb_merge_shard_payload(payload, M, k, surface, temperature, out: sb_outputs,
+                           stream=None) -> int:
+    return int(lib().sb_merge_shard_payload(_ptr(payload), M, k, surface, float(temperature),
+                                            ctypes.byref(out), _stream(stream)))
 
 
 def sb_last_device_status(out: sb_outputs) -> int:

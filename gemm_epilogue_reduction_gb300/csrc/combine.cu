@@ -144,12 +144,110 @@ __global__ void __launch_bounds__(32 * kMaxWarps) combine_kernel(const CombinePa
     }
 }
 
-// Top-K: per (row, shard) warp, lane l keeps a sorted list (largest first, equal values by
-// ascending column) of the kMaxTopK best entries of its tiles l, l+32, ... (tiles, and the
-// entries within a tile, arrive in ascending column order, so an equal value already kept
-// has the lower column); then K rounds of a warp-wide max over the lanes' list heads give
-// the shard's top K.  Thread 0 merges the k shard lists the same way.  Selection compares
-// values only, so the result is the same for any order of these steps.
+// ------------------------------------------------------------------ shard payloads
+// The record a vocabulary lane would send to the others: its shard-local completion, with
+// columns made global by `col_offset`.  Payload layout: lane-major, record (s, r) at
+// index s * M + r; 12 bytes (m, idx, s), plus (gkey, gidx, gz) for the Gumbel surface.
+struct PayloadParams {
+    int M, k, T;
+    int gumbel;
+    long long col_offset;
+    Workspace ws;
+    unsigned char *payload;
+};
+
+template <bool GUMBEL>
+__global__ void __launch_bounds__(32 * kMaxWarps) pack_kernel(const PayloadParams p) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int row = blockIdx.x;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int sh_i = warp; sh_i < p.k; sh_i += nwarps) {
+        Rec r{-INFINITY, INT_MAX, 0.f};
+        GRec g{-INFINITY, INT_MAX, 0.f};
+        const size_t base = (static_cast<size_t>(row) * p.k + sh_i) * p.T;
+        for (int t0 = lane; t0 < p.T; t0 += 32 * kBatch) {
+            Rec x[kBatch];
+            GRec y[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int t = t0 + 32 * u;
+                if (t < p.T) {
+                    x[u] = Rec{__ldg(p.ws.m + base + t), __ldg(p.ws.idx + base + t),
+                               __ldg(p.ws.s + base + t)};
+                    if (GUMBEL)
+                        y[u] = GRec{__ldg(p.ws.gk + base + t), __ldg(p.ws.gi + base + t),
+                                    __ldg(p.ws.gz + base + t)};
+                } else {
+                    x[u] = Rec{-INFINITY, INT_MAX, 0.f};
+                    if (GUMBEL) y[u] = GRec{-INFINITY, INT_MAX, 0.f};
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                r = merge(r, x[u]);
+                if (GUMBEL) g = gmerge(g, y[u]);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const Rec o{__shfl_xor_sync(0xFFFFFFFFu, r.m, off),
+                        __shfl_xor_sync(0xFFFFFFFFu, r.i, off),
+                        __shfl_xor_sync(0xFFFFFFFFu, r.s, off)};
+            r = merge(r, o);
+            if (GUMBEL) {
+                const GRec go{__shfl_xor_sync(0xFFFFFFFFu, g.k, off),
+                              __shfl_xor_sync(0xFFFFFFFFu, g.i, off),
+                              __shfl_xor_sync(0xFFFFFFFFu, g.z, off)};
+                g = gmerge(g, go);
+            }
+        }
+        if (lane == 0) {
+            const size_t rec = static_cast<size_t>(sh_i) * p.M + row;
+            float *f = reinterpret_cast<float *>(p.payload + rec * (GUMBEL ? 24 : 12));
+            int *i = reinterpret_cast<int *>(f);
+            f[0] = r.m;
+            i[1] = r.i == INT_MAX ? INT_MAX : static_cast<int>(r.i + p.col_offset);
+            f[2] = r.s;
+            if (GUMBEL) {
+                f[3] = g.k;
+                i[4] = g.i == INT_MAX ? INT_MAX : static_cast<int>(g.i + p.col_offset);
+                f[5] = g.z;
+            }
+        }
+    }
+}
+
+template <bool GUMBEL>
+__global__ void merge_payload_kernel(const CombineParams c, const unsigned char *payload) {
+    const int row = blockIdx.x * blockDim.x + threadIdx.x;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (row >= c.M) return;
+    Rec acc{-INFINITY, INT_MAX, 0.f};
+    GRec gacc{-INFINITY, INT_MAX, 0.f};
+    for (int s2 = 0; s2 < c.k; ++s2) {
+        const size_t rec = static_cast<size_t>(s2) * c.M + row;
+        const float *f = reinterpret_cast<const float *>(payload + rec * (GUMBEL ? 24 : 12));
+        const int *i = reinterpret_cast<const int *>(f);
+        acc = merge(acc, Rec{f[0], i[1], f[2]});
+        if (GUMBEL) gacc = gmerge(gacc, GRec{f[3], i[4], f[5]});
+    }
+    const float lse = acc.m + logf(acc.s);
+    c.token[row] = GUMBEL ? gacc.i : acc.i;
+    if (c.lse) c.lse[row] = lse;
+    if (c.token_logprob) c.token_logprob[row] = GUMBEL ? gacc.z * c.inv_t - lse : -logf(acc.s);
+}
+
+// Top-K: one block per row; all its warps work on one shard at a time.  Thread t folds the
+// records of tiles t, t + 256, ... into (a) a running (m, i, s) record and (b) a sorted list
+// (largest first, equal values by ascending column) of the kMaxTopK best entries -- tiles,
+// and the entries within a tile, arrive in ascending column order, so an equal value
+// already kept has the lower column.  Each warp then takes its K best by K rounds of a
+// warp-wide max over its lanes' list heads, and one warp takes the shard's K best from the
+// warps' lists the same way.  (m, i, s) reduces by the xor butterfly and the warps' results
+// merge in warp order.  Thread 0 finally merges the k shard results.  Selection compares
+// values only, so its result does not depend on this order.
 __device__ __forceinline__ uint32_t ord_f(float f) {
     const uint32_t u = __float_as_uint(f);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
@@ -158,20 +256,72 @@ __device__ __forceinline__ float unord_f(uint32_t o) {
     return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
 }
 
+// K rounds of warp max over the lanes' sorted lists (tv, ti) of kMaxTopK entries; lane 0
+// writes the winners to (ov, oi).  Lanes with nothing hold (-inf, INT_MAX) heads.
+__device__ __forceinline__ void warp_select(const float (&tv)[kMaxTopK], const int (&ti)[kMaxTopK],
+                                            int K, float *ov, int *oi) {
+    const int lane = threadIdx.x & 31;
+    int hp = 0;
+    for (int q = 0; q < K; ++q) {
+        float hv = -INFINITY;
+        int hi = INT_MAX;
+#pragma unroll
+        for (int e = 0; e < kMaxTopK; ++e)
+            if (e == hp) {
+                hv = tv[e];
+                hi = ti[e];
+            }
+        const uint32_t oh = ord_f(hv);
+        const uint32_t om = __reduce_max_sync(0xFFFFFFFFu, oh);
+        const int wi = __reduce_min_sync(0xFFFFFFFFu, oh == om ? hi : INT_MAX);
+        if (oh == om && hi == wi && hp < kMaxTopK) ++hp;
+        if (lane == 0) {
+            ov[q] = unord_f(om);
+            oi[q] = wi;
+        }
+    }
+}
+
+__device__ __forceinline__ void list_insert(float (&tv)[kMaxTopK], int (&ti)[kMaxTopK], float x,
+                                            int xi) {
+    float cv = x;
+    int ci = xi;
+    bool ins = false;
+#pragma unroll
+    for (int q = 0; q < kMaxTopK; ++q) {
+        if (ins || cv > tv[q]) {
+            const float a = tv[q];
+            const int b = ti[q];
+            tv[q] = cv;
+            ti[q] = ci;
+            cv = a;
+            ci = b;
+            ins = true;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(32 * kMaxWarps) combine_topk_kernel(const CombineParams p) {
-    extern __shared__ float sh[];  // k x (m, i, s), then k x K values, k x K columns
+    // shared: k x (m, i, s); k x K shard lists (values, columns); 8 x K warp lists; 8 x 3
+    extern __shared__ float sh[];
+    const int K = p.topk;
     float *sm = sh;
     int *si = reinterpret_cast<int *>(sh + p.k);
     float *ss = sh + 2 * p.k;
-    const int K = p.topk;
     float *slv = sh + 3 * p.k;
     int *sli = reinterpret_cast<int *>(slv + p.k * K);
+    float *wlv = reinterpret_cast<float *>(sli + p.k * K);
+    int *wli = reinterpret_cast<int *>(wlv + kMaxWarps * K);
+    float *wm = reinterpret_cast<float *>(wli + kMaxWarps * K);
+    int *wmi = reinterpret_cast<int *>(wm + kMaxWarps);
+    float *wms = wm + 2 * kMaxWarps;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int nwarps = blockDim.x >> 5;
+    const int nthreads = blockDim.x;
+    const int nwarps = nthreads >> 5;
     const int row = blockIdx.x;
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (int sh_i = warp; sh_i < p.k; sh_i += nwarps) {
+    for (int sh_i = 0; sh_i < p.k; ++sh_i) {
         Rec r{-INFINITY, INT_MAX, 0.f};
         float tv[kMaxTopK];
         int ti[kMaxTopK];
@@ -181,29 +331,22 @@ __global__ void __launch_bounds__(32 * kMaxWarps) combine_topk_kernel(const Comb
             ti[q] = INT_MAX;
         }
         const size_t base = (static_cast<size_t>(row) * p.k + sh_i) * p.T;
-        for (int t = lane; t < p.T; t += 32) {
-            r = merge(r, Rec{__ldg(p.ws.m + base + t), __ldg(p.ws.idx + base + t),
-                             __ldg(p.ws.s + base + t)});
+        for (int t = threadIdx.x; t < p.T; t += nthreads) {
+            // issue every load of the record before using any of them
+            const Rec rec{__ldg(p.ws.m + base + t), __ldg(p.ws.idx + base + t),
+                          __ldg(p.ws.s + base + t)};
             const size_t o = (base + t) * K;
-            for (int e = 0; e < K; ++e) {
-                const float x = __ldg(p.ws.tkv + o + e);
-                if (!(x > tv[kMaxTopK - 1])) break;  // entries are sorted: the rest lose too
-                float cv = x;
-                int ci = __ldg(p.ws.tki + o + e);
-                bool ins = false;
+            float xv[kMaxTopK];
+            int xi[kMaxTopK];
 #pragma unroll
-                for (int q = 0; q < kMaxTopK; ++q) {
-                    if (ins || cv > tv[q]) {
-                        const float a = tv[q];
-                        const int b = ti[q];
-                        tv[q] = cv;
-                        ti[q] = ci;
-                        cv = a;
-                        ci = b;
-                        ins = true;
-                    }
-                }
+            for (int e = 0; e < kMaxTopK; ++e) {
+                xv[e] = e < K ? __ldg(p.ws.tkv + o + e) : -INFINITY;
+                xi[e] = e < K ? __ldg(p.ws.tki + o + e) : INT_MAX;
             }
+            r = merge(r, rec);
+#pragma unroll
+            for (int e = 0; e < kMaxTopK; ++e)
+                if (xv[e] > tv[kMaxTopK - 1]) list_insert(tv, ti, xv[e], xi[e]);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
@@ -212,31 +355,34 @@ __global__ void __launch_bounds__(32 * kMaxWarps) combine_topk_kernel(const Comb
                         __shfl_xor_sync(0xFFFFFFFFu, r.s, off)};
             r = merge(r, o);
         }
-        int hp = 0;  // this lane's list head
-        for (int q = 0; q < K; ++q) {
-            float hv = -INFINITY;
-            int hi = INT_MAX;
+        warp_select(tv, ti, K, wlv + warp * K, wli + warp * K);
+        if (lane == 0) {
+            wm[warp] = r.m;
+            wmi[warp] = r.i;
+            wms[warp] = r.s;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // lane w < nwarps owns warp w's sorted list (its first K entries)
+            float lv[kMaxTopK];
+            int li[kMaxTopK];
 #pragma unroll
-            for (int e = 0; e < kMaxTopK; ++e)
-                if (e == hp) {
-                    hv = tv[e];
-                    hi = ti[e];
-                }
-            const uint32_t om = __reduce_max_sync(0xFFFFFFFFu, ord_f(hv));
-            const int wi = __reduce_min_sync(0xFFFFFFFFu, ord_f(hv) == om ? hi : INT_MAX);
-            if (hi == wi && ord_f(hv) == om && hp < kMaxTopK) ++hp;
+            for (int q = 0; q < kMaxTopK; ++q) {
+                const bool have = lane < nwarps && q < K;
+                lv[q] = have ? wlv[lane * K + q] : -INFINITY;
+                li[q] = have ? wli[lane * K + q] : INT_MAX;
+            }
+            warp_select(lv, li, K, slv + sh_i * K, sli + sh_i * K);
             if (lane == 0) {
-                slv[sh_i * K + q] = unord_f(om);
-                sli[sh_i * K + q] = wi;
+                Rec acc{-INFINITY, INT_MAX, 0.f};
+                for (int w = 0; w < nwarps; ++w) acc = merge(acc, Rec{wm[w], wmi[w], wms[w]});
+                sm[sh_i] = acc.m;
+                si[sh_i] = acc.i;
+                ss[sh_i] = acc.s;
             }
         }
-        if (lane == 0) {
-            sm[sh_i] = r.m;
-            si[sh_i] = r.i;
-            ss[sh_i] = r.s;
-        }
+        __syncthreads();
     }
-    __syncthreads();
     if (threadIdx.x != 0) return;
     Rec acc{-INFINITY, INT_MAX, 0.f};
     for (int s2 = 0; s2 < p.k; ++s2) acc = merge(acc, Rec{sm[s2], si[s2], ss[s2]});
@@ -245,8 +391,7 @@ __global__ void __launch_bounds__(32 * kMaxWarps) combine_topk_kernel(const Comb
     if (p.lse) p.lse[row] = lse;
     if (p.token_logprob) p.token_logprob[row] = -logf(acc.s);
     if (p.target_logprob) p.target_logprob[row] = p.ws.tz[row] - lse;
-    // k-way merge of the sorted shard lists; the heads are kept in the first k ints of the
-    // shard (m) array, no longer needed
+    // k-way merge of the sorted shard lists; the heads reuse the (no longer needed) m array
     int *heads = reinterpret_cast<int *>(sm);
     for (int s2 = 0; s2 < p.k; ++s2) heads[s2] = 0;
     for (int q = 0; q < K; ++q) {
@@ -283,11 +428,57 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (p.flags & kFlagTopk) {
-        cfg.dynamicSmemBytes = static_cast<size_t>(p.k) * (12 + 8 * p.topk);
+        cfg.blockDim = dim3(32 * kMaxWarps);
+        cfg.dynamicSmemBytes = static_cast<size_t>(p.k) * (12 + 8 * p.topk) +
+                               static_cast<size_t>(kMaxWarps) * (8 * p.topk + 12);
         return cudaLaunchKernelEx(&cfg, combine_topk_kernel, p);
     }
     if (p.flags & kFlagGumbel) return cudaLaunchKernelEx(&cfg, combine_kernel<true>, p);
     return cudaLaunchKernelEx(&cfg, combine_kernel<false>, p);
+}
+
+}  // namespace sb
+
+namespace sb {
+
+cudaError_t launch_pack(const Workspace &ws, int M, int k, int T, bool gumbel,
+                        long long col_offset, void *payload, cudaStream_t stream) {
+    PayloadParams p{};
+    p.M = M;
+    p.k = k;
+    p.T = T;
+    p.gumbel = gumbel;
+    p.col_offset = col_offset;
+    p.ws = ws;
+    p.payload = static_cast<unsigned char *>(payload);
+    const int warps = k < kMaxWarps ? k : kMaxWarps;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(M);
+    cfg.blockDim = dim3(32 * warps);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (gumbel) return cudaLaunchKernelEx(&cfg, pack_kernel<true>, p);
+    return cudaLaunchKernelEx(&cfg, pack_kernel<false>, p);
+}
+
+cudaError_t launch_merge_payload(const CombineParams &c, const void *payload,
+                                 cudaStream_t stream) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((c.M + 127) / 128);
+    cfg.blockDim = dim3(128);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const unsigned char *pl = static_cast<const unsigned char *>(payload);
+    if (c.flags & kFlagGumbel) return cudaLaunchKernelEx(&cfg, merge_payload_kernel<true>, c, pl);
+    return cudaLaunchKernelEx(&cfg, merge_payload_kernel<false>, c, pl);
 }
 
 }  // namespace sb

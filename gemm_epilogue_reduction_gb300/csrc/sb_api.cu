@@ -370,6 +370,58 @@ int32_t sb_combine_shard_records(const void *workspace, int64_t M, int32_t k,
     return SB_OK;
 }
 
+size_t sb_payload_bytes(int64_t M, int32_t k, int32_t surface) {
+    if (M < 1 || M > (int64_t(1) << 30) || k < 1 || k > kMaxShards) return 0;
+    if (surface != SB_TOKEN && surface != SB_TOKEN_LOGPROB && surface != SB_FULL_LOGITS &&
+        surface != SB_GUMBEL_TOKEN)
+        return 0;
+    return static_cast<size_t>(M) * k * (surface == SB_GUMBEL_TOKEN ? 24 : 12);
+}
+
+int32_t sb_pack_shard_records(const void *workspace, int64_t M, int32_t k,
+                              int32_t tiles_per_shard_, int32_t surface, int64_t col_offset,
+                              void *payload, void *stream) {
+    const size_t pb = sb_payload_bytes(M, k, surface);
+    if (!workspace || !payload || pb == 0 || tiles_per_shard_ < 1 || col_offset < 0 ||
+        col_offset >= (int64_t(1) << 31))
+        return SB_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256) || !aligned(payload, 4)) return SB_ERR_ALIGNMENT;
+    DevInfo dev;
+    if (int32_t e = current_device(&dev)) return e;
+    const bool gumbel = surface == SB_GUMBEL_TOKEN;
+    const WsLayout L = ws_layout(M, k, tiles_per_shard_, gumbel);
+    const Workspace w = ws_views(const_cast<void *>(workspace), L, gumbel);
+    if (launch_pack(w, static_cast<int>(M), k, tiles_per_shard_, gumbel, col_offset, payload,
+                    static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SB_ERR_CUDA;
+    return SB_OK;
+}
+
+int32_t sb_merge_shard_payload(const void *payload, int64_t M, int32_t k, int32_t surface,
+                               float temperature, const sb_outputs *out, void *stream) {
+    if (!payload || sb_payload_bytes(M, k, surface) == 0 || !out || !out->token)
+        return SB_ERR_INVALID_ARG;
+    const bool gumbel = surface == SB_GUMBEL_TOKEN;
+    if (gumbel && !(std::isfinite(temperature) && temperature > 0.f)) return SB_ERR_INVALID_ARG;
+    if ((surface == SB_TOKEN_LOGPROB || gumbel) && !out->token_logprob) return SB_ERR_INVALID_ARG;
+    if (!aligned(payload, 4) || !aligned(out->token, 4) || !aligned(out->token_logprob, 4) ||
+        !aligned(out->lse, 4))
+        return SB_ERR_ALIGNMENT;
+    DevInfo dev;
+    if (int32_t e = current_device(&dev)) return e;
+    CombineParams c{};
+    c.M = static_cast<int>(M);
+    c.k = k;
+    c.flags = gumbel ? kFlagGumbel : 0;
+    c.inv_t = gumbel ? 1.0f / temperature : 1.0f;
+    c.token = out->token;
+    c.token_logprob = out->token_logprob;
+    c.lse = out->lse;
+    if (launch_merge_payload(c, payload, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SB_ERR_CUDA;
+    return SB_OK;
+}
+
 int32_t sb_last_device_status(const sb_outputs *out) {
     if (!out || !out->workspace || out->workspace_bytes < 16) return SB_ERR_INVALID_ARG;
     uint64_t hdr[2] = {0, 0};

@@ -91,6 +91,10 @@ struct CombineParams {
 cudaError_t launch_lmhead(bool vocab_mode, const CUtensorMap &tmA, const CUtensorMap &tmB,
                           const GemmParams &p, size_t smem, int num_sms, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
+cudaError_t launch_pack(const Workspace &ws, int M, int k, int T, bool gumbel,
+                        long long col_offset, void *payload, cudaStream_t stream);
+cudaError_t launch_merge_payload(const CombineParams &c, const void *payload,
+                                 cudaStream_t stream);
 
 size_t lmhead_smem_bytes(int nb, int stages_a, int stages_b, bool vocab_mode, int flags);
 

@@ -214,6 +214,40 @@ int32_t sb_lmhead_project_static_scratch(const void *H, const void *W, int64_t M
  * enqueued on stream. */
 int32_t sb_debug_gumbel_from_bits(const uint32_t *bits, float *g, int64_t count, void *stream);
 
+/*
+ * Shard payloads: what each vocabulary lane would send to the others instead of its logit
+ * slice (Figure 1 and Section 5.2: full-logit transfer ships V logit elements in k frames,
+ * source projection ships the per-lane projection).  A lane's payload is its shard-local
+ * completion: per row one record (m, idx, s) = (max logit, lowest global column attaining
+ * it, sum of exp(z - m)) -- 12 bytes; the Gumbel surface adds (gkey, gidx, gz) -- 24 bytes.
+ * The top-K surface has no payload form.
+ * Layout: lane-major, record (lane s, row r) at byte (s * M + r) * record_bytes; fields are
+ * float32 / int32 in that order.  Merging the k payloads in ascending lane order gives the
+ * same bits as sb_combine_shard_records on the same records.
+ */
+
+/* k * M * record_bytes for the surfaces above; 0 for invalid arguments or SB_TOPK_LOGPROB. */
+size_t sb_payload_bytes(int64_t M, int32_t k, int32_t surface);
+
+/*
+ * Shard-local completion of the k lanes' records in `workspace` (as left by
+ * sb_lmhead_records for M, k and T = tiles_per_shard) into `payload` (device, 4-byte
+ * aligned, sb_payload_bytes(M, k, surface) bytes), adding col_offset (>= 0) to every column
+ * so that a caller holding only a slice of W (for example one device of a
+ * vocabulary-sharded head) produces global columns.  Enqueued on stream.
+ */
+int32_t sb_pack_shard_records(const void *workspace, int64_t M, int32_t k,
+                              int32_t tiles_per_shard, int32_t surface, int64_t col_offset,
+                              void *payload, void *stream);
+
+/*
+ * Cross-lane merge of k lane payloads (device, lane-major as above): writes out->token and,
+ * where non-NULL, out->token_logprob and out->lse (target log-probs are not carried by the
+ * payload; out->workspace is not used).  temperature as for sb_lmhead_project.
+ */
+int32_t sb_merge_shard_payload(const void *payload, int64_t M, int32_t k, int32_t surface,
+                               float temperature, const sb_outputs *out, void *stream);
+
 /* Device status of the last call that used out->workspace: SB_OK or
  * SB_ERR_DEVICE_TIMEOUT.  Synchronous: copies the header to the host (call it after
  * synchronising the stream).  Returns SB_ERR_CUDA if the copy fails. */
