@@ -239,15 +239,7 @@ __global__ void merge_payload_kernel(const CombineParams c, const unsigned char 
     if (c.token_logprob) c.token_logprob[row] = GUMBEL ? gacc.z * c.inv_t - lse : -logf(acc.s);
 }
 
-// Top-K: one block per row; all its warps work on one shard at a time.  Thread t folds the
-// records of tiles t, t + 256, ... into (a) a running (m, i, s) record and (b) a sorted list
-// (largest first, equal values by ascending column) of the kMaxTopK best entries -- tiles,
-// and the entries within a tile, arrive in ascending column order, so an equal value
-// already kept has the lower column.  Each warp then takes its K best by K rounds of a
-// warp-wide max over its lanes' list heads, and one warp takes the shard's K best from the
-// warps' lists the same way.  (m, i, s) reduces by the xor butterfly and the warps' results
-// merge in warp order.  Thread 0 finally merges the k shard results.  Selection compares
-// values only, so its result does not depend on this order.
+// ------------------------------------------------------------------ top-K helpers
 __device__ __forceinline__ uint32_t ord_f(float f) {
     const uint32_t u = __float_as_uint(f);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
@@ -301,52 +293,78 @@ __device__ __forceinline__ void list_insert(float (&tv)[kMaxTopK], int (&ti)[kMa
     }
 }
 
+// Rank of (v, i) against (tv, ti) in the surface's order (larger value first, then lower
+// column): true if (v, i) ranks at or above.
+__device__ __forceinline__ bool ranks_at_or_above(float v, int i, float tv, int ti) {
+    return v > tv || (v == tv && i <= ti);
+}
+
+// Block-wide top-K of the threads' sorted lists: each warp picks its K best, then warp 0
+// picks the K best of the warps' lists into (ov, oi) in shared memory.
+__device__ __forceinline__ void block_select(const float (&tv)[kMaxTopK], const int (&ti)[kMaxTopK],
+                                             int K, float *wlv, int *wli, float *ov, int *oi) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    warp_select(tv, ti, K, wlv + warp * K, wli + warp * K);
+    __syncthreads();
+    if (warp == 0) {
+        float lv[kMaxTopK];
+        int li[kMaxTopK];
+#pragma unroll
+        for (int q = 0; q < kMaxTopK; ++q) {
+            const bool have = lane < nwarps && q < K;
+            lv[q] = have ? wlv[lane * K + q] : -INFINITY;
+            li[q] = have ? wli[lane * K + q] : INT_MAX;
+        }
+        warp_select(lv, li, K, ov, oi);
+    }
+    __syncthreads();
+}
+
+// Top-K combine, one block per row.
+//  1. lse and token: exactly the fixed tree of the plain combine (so they equal the token
+//     surface's bits): warps over shards, lanes over tiles, xor butterfly, shards ascending.
+//  2. theta = the K-th largest of the row's tile maxima.  The K tiles whose maxima rank at
+//     or above theta hold K distinct entries that do, so no entry ranking below theta can
+//     be in the row's top K.
+//  3. Only records whose maximum ranks at or above theta are read; their entries ranking
+//     at or above theta are the candidates, and the block selects the K best of them.
+// Each thread walks its records in ascending column order, so an equal value already in
+// its list has the lower column (list_insert keeps it first).  Selection compares values
+// only, so the result does not depend on how the work is split.
 __global__ void __launch_bounds__(32 * kMaxWarps) combine_topk_kernel(const CombineParams p) {
-    // shared: k x (m, i, s); k x K shard lists (values, columns); 8 x K warp lists; 8 x 3
-    extern __shared__ float sh[];
+    extern __shared__ float sh[];  // k x (m, i, s); 8 x K warp lists; 2 x K block lists; theta
     const int K = p.topk;
     float *sm = sh;
     int *si = reinterpret_cast<int *>(sh + p.k);
     float *ss = sh + 2 * p.k;
-    float *slv = sh + 3 * p.k;
-    int *sli = reinterpret_cast<int *>(slv + p.k * K);
-    float *wlv = reinterpret_cast<float *>(sli + p.k * K);
+    float *wlv = sh + 3 * p.k;
     int *wli = reinterpret_cast<int *>(wlv + kMaxWarps * K);
-    float *wm = reinterpret_cast<float *>(wli + kMaxWarps * K);
-    int *wmi = reinterpret_cast<int *>(wm + kMaxWarps);
-    float *wms = wm + 2 * kMaxWarps;
+    float *blv = reinterpret_cast<float *>(wli + kMaxWarps * K);
+    int *bli = reinterpret_cast<int *>(blv + K);
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
     const int nthreads = blockDim.x;
-    const int nwarps = nthreads >> 5;
     const int row = blockIdx.x;
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (int sh_i = 0; sh_i < p.k; ++sh_i) {
+
+    // 1. shard records (the plain combine's tree)
+    for (int sh_i = warp; sh_i < p.k; sh_i += nwarps) {
         Rec r{-INFINITY, INT_MAX, 0.f};
-        float tv[kMaxTopK];
-        int ti[kMaxTopK];
-#pragma unroll
-        for (int q = 0; q < kMaxTopK; ++q) {
-            tv[q] = -INFINITY;
-            ti[q] = INT_MAX;
-        }
         const size_t base = (static_cast<size_t>(row) * p.k + sh_i) * p.T;
-        for (int t = threadIdx.x; t < p.T; t += nthreads) {
-            // issue every load of the record before using any of them
-            const Rec rec{__ldg(p.ws.m + base + t), __ldg(p.ws.idx + base + t),
-                          __ldg(p.ws.s + base + t)};
-            const size_t o = (base + t) * K;
-            float xv[kMaxTopK];
-            int xi[kMaxTopK];
+        for (int t0 = lane; t0 < p.T; t0 += 32 * kBatch) {
+            Rec x[kBatch];
 #pragma unroll
-            for (int e = 0; e < kMaxTopK; ++e) {
-                xv[e] = e < K ? __ldg(p.ws.tkv + o + e) : -INFINITY;
-                xi[e] = e < K ? __ldg(p.ws.tki + o + e) : INT_MAX;
+            for (int u = 0; u < kBatch; ++u) {
+                const int t = t0 + 32 * u;
+                x[u] = t < p.T ? Rec{__ldg(p.ws.m + base + t), __ldg(p.ws.idx + base + t),
+                                     __ldg(p.ws.s + base + t)}
+                               : Rec{-INFINITY, INT_MAX, 0.f};
             }
-            r = merge(r, rec);
 #pragma unroll
-            for (int e = 0; e < kMaxTopK; ++e)
-                if (xv[e] > tv[kMaxTopK - 1]) list_insert(tv, ti, xv[e], xi[e]);
+            for (int u = 0; u < kBatch; ++u) r = merge(r, x[u]);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
@@ -355,34 +373,57 @@ __global__ void __launch_bounds__(32 * kMaxWarps) combine_topk_kernel(const Comb
                         __shfl_xor_sync(0xFFFFFFFFu, r.s, off)};
             r = merge(r, o);
         }
-        warp_select(tv, ti, K, wlv + warp * K, wli + warp * K);
         if (lane == 0) {
-            wm[warp] = r.m;
-            wmi[warp] = r.i;
-            wms[warp] = r.s;
+            sm[sh_i] = r.m;
+            si[sh_i] = r.i;
+            ss[sh_i] = r.s;
         }
-        __syncthreads();
-        if (warp == 0) {
-            // lane w < nwarps owns warp w's sorted list (its first K entries)
-            float lv[kMaxTopK];
-            int li[kMaxTopK];
-#pragma unroll
-            for (int q = 0; q < kMaxTopK; ++q) {
-                const bool have = lane < nwarps && q < K;
-                lv[q] = have ? wlv[lane * K + q] : -INFINITY;
-                li[q] = have ? wli[lane * K + q] : INT_MAX;
-            }
-            warp_select(lv, li, K, slv + sh_i * K, sli + sh_i * K);
-            if (lane == 0) {
-                Rec acc{-INFINITY, INT_MAX, 0.f};
-                for (int w = 0; w < nwarps; ++w) acc = merge(acc, Rec{wm[w], wmi[w], wms[w]});
-                sm[sh_i] = acc.m;
-                si[sh_i] = acc.i;
-                ss[sh_i] = acc.s;
-            }
-        }
-        __syncthreads();
     }
+
+    // 2. theta from the tile maxima (a row's records are contiguous: f = s * T + t)
+    const int nrec = p.k * p.T;
+    const size_t rbase = static_cast<size_t>(row) * nrec;
+    float tv[kMaxTopK];
+    int ti[kMaxTopK];
+#pragma unroll
+    for (int q = 0; q < kMaxTopK; ++q) {
+        tv[q] = -INFINITY;
+        ti[q] = INT_MAX;
+    }
+    for (int f = threadIdx.x; f < nrec; f += nthreads) {
+        const float m = __ldg(p.ws.m + rbase + f);
+        if (m > tv[kMaxTopK - 1]) list_insert(tv, ti, m, __ldg(p.ws.idx + rbase + f));
+    }
+    block_select(tv, ti, K, wlv, wli, blv, bli);
+    const float th_v = blv[K - 1];  // -inf / INT_MAX when the row has fewer than K tiles
+    const int th_i = bli[K - 1];
+
+    // 3. candidates at or above theta
+#pragma unroll
+    for (int q = 0; q < kMaxTopK; ++q) {
+        tv[q] = -INFINITY;
+        ti[q] = INT_MAX;
+    }
+    for (int f = threadIdx.x; f < nrec; f += nthreads) {
+        const float m = __ldg(p.ws.m + rbase + f);
+        const int mi = __ldg(p.ws.idx + rbase + f);
+        if (!ranks_at_or_above(m, mi, th_v, th_i) && th_v != -INFINITY) continue;
+        const size_t o = (rbase + f) * K;
+        float xv[kMaxTopK];
+        int xi[kMaxTopK];
+#pragma unroll
+        for (int e = 0; e < kMaxTopK; ++e) {
+            xv[e] = e < K ? __ldg(p.ws.tkv + o + e) : -INFINITY;
+            xi[e] = e < K ? __ldg(p.ws.tki + o + e) : INT_MAX;
+        }
+#pragma unroll
+        for (int e = 0; e < kMaxTopK; ++e)
+            if (xv[e] > tv[kMaxTopK - 1] &&
+                (th_v == -INFINITY || ranks_at_or_above(xv[e], xi[e], th_v, th_i)))
+                list_insert(tv, ti, xv[e], xi[e]);
+    }
+    block_select(tv, ti, K, wlv, wli, blv, bli);
+
     if (threadIdx.x != 0) return;
     Rec acc{-INFINITY, INT_MAX, 0.f};
     for (int s2 = 0; s2 < p.k; ++s2) acc = merge(acc, Rec{sm[s2], si[s2], ss[s2]});
@@ -391,25 +432,9 @@ __global__ void __launch_bounds__(32 * kMaxWarps) combine_topk_kernel(const Comb
     if (p.lse) p.lse[row] = lse;
     if (p.token_logprob) p.token_logprob[row] = -logf(acc.s);
     if (p.target_logprob) p.target_logprob[row] = p.ws.tz[row] - lse;
-    // k-way merge of the sorted shard lists; the heads reuse the (no longer needed) m array
-    int *heads = reinterpret_cast<int *>(sm);
-    for (int s2 = 0; s2 < p.k; ++s2) heads[s2] = 0;
     for (int q = 0; q < K; ++q) {
-        float bv = -INFINITY;
-        int bi = INT_MAX, bs = -1;
-        for (int s2 = 0; s2 < p.k; ++s2) {
-            if (heads[s2] >= K) continue;
-            const float v = slv[s2 * K + heads[s2]];
-            const int i = sli[s2 * K + heads[s2]];
-            if (v > bv || (v == bv && i < bi)) {
-                bv = v;
-                bi = i;
-                bs = s2;
-            }
-        }
-        if (bs >= 0) ++heads[bs];
-        p.topk_ids[static_cast<size_t>(row) * K + q] = bi;
-        p.topk_logprob[static_cast<size_t>(row) * K + q] = bv - lse;
+        p.topk_ids[static_cast<size_t>(row) * K + q] = bli[q];
+        p.topk_logprob[static_cast<size_t>(row) * K + q] = blv[q] - lse;
     }
 }
 
@@ -429,8 +454,8 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
     cfg.numAttrs = 1;
     if (p.flags & kFlagTopk) {
         cfg.blockDim = dim3(32 * kMaxWarps);
-        cfg.dynamicSmemBytes = static_cast<size_t>(p.k) * (12 + 8 * p.topk) +
-                               static_cast<size_t>(kMaxWarps) * (8 * p.topk + 12);
+        cfg.dynamicSmemBytes = static_cast<size_t>(p.k) * 12 +
+                               static_cast<size_t>(kMaxWarps + 1) * 8 * p.topk;
         return cudaLaunchKernelEx(&cfg, combine_topk_kernel, p);
     }
     if (p.flags & kFlagGumbel) return cudaLaunchKernelEx(&cfg, combine_kernel<true>, p);

@@ -91,3 +91,16 @@ def test_topk_decode_shape():
     torch.cuda.synchronize()
     assert sb.sb_last_device_status(res["_outputs"]) == sb.SB_OK
     check_topk(res, H, W, K)
+
+
+@pytest.mark.parametrize("M,d,V,k", [(16, 256, 4096, 4), (300, 64, 2000, 2)])
+def test_topk_surface_token_and_lse_bits_equal_the_token_surface(M, d, V, k):
+    """The top-K combine completes lse and the token with the same fixed tree as the token
+    surface, so those outputs agree bit for bit."""
+    H, W = synth.make_hw(M, d, V, seed=31)
+    H, W = H.cuda(), W.cuda()
+    a = sb.project(H, W, k, sb.SB_TOPK_LOGPROB, topk=6)
+    b = sb.project(H, W, k, sb.SB_TOKEN_LOGPROB)
+    torch.cuda.synchronize()
+    for key in ("token", "token_logprob", "lse"):
+        assert torch.equal(a[key], b[key]), key
