@@ -42,6 +42,7 @@
 
 #include "sb_gumbel.cuh"
 #include "sb_internal.h"
+#include "sb_pipe.cuh"
 #include "sb_ptx.cuh"
 
 namespace sb {
@@ -49,7 +50,6 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kStageBytesA = kTileA * kBlockK * 2;  // 16 KB
-constexpr uint32_t kTimeoutCode = 6;                      // SB_ERR_DEVICE_TIMEOUT
 
 struct SmemLayout {
     uint32_t a_off, b_off, bar_off, misc_off, tgt_off, scratch_off, total;
@@ -101,41 +101,16 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams &p, int tile, i
     return c;
 }
 
-__device__ __noinline__ void raise_timeout(const GemmParams &p, volatile int *abort_flag) {
-    *abort_flag = 1;
-    atomicMax(p.ws.status, (static_cast<unsigned long long>(p.epoch) << 32) | kTimeoutCode);
+__device__ __forceinline__ WaitCtx wait_ctx(const GemmParams &p, volatile int *abort_flag) {
+    return WaitCtx{p.ws.status, p.epoch, p.timeout_ns, abort_flag};
 }
-
-// Bounded wait on an mbarrier phase.  Returns false when the CTA is aborting (another
-// role gave up) or when this wait itself runs out of time.
 __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                       const GemmParams &p) {
-    if (mbar_test(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_test(bar, parity)) return true;
-        if ((i & 63u) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > p.timeout_ns) {
-                raise_timeout(p, abort_flag);
-                return false;
-            }
-        }
-    }
+    return bwait(bar, parity, wait_ctx(p, abort_flag));
 }
-
-// Bounded wait used while draining: ignores the abort flag (the copies or MMAs being
-// waited for complete on their own), but still gives up after the time limit.
 __device__ __forceinline__ void bwait_drain(uint64_t *bar, uint32_t parity,
                                             volatile int *abort_flag, const GemmParams &p) {
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 0;; ++i) {
-        if (mbar_test(bar, parity)) return;
-        if ((i & 63u) == 63u && globaltimer_ns() - t0 > p.timeout_ns) {
-            raise_timeout(p, abort_flag);
-            return;
-        }
-    }
+    bwait_drain(bar, parity, wait_ctx(p, abort_flag));
 }
 
 __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }

@@ -1,0 +1,57 @@
+// sb_pipe.cuh -- the time-bounded mbarrier waits shared by the pipelined kernels.
+//
+// Every wait polls with mbarrier.try_wait and gives up after a %globaltimer limit: it then
+// records SB_ERR_DEVICE_TIMEOUT (tagged with the launch epoch) in the caller-visible status
+// word and raises a CTA-wide abort flag that the other roles' waits notice.
+#pragma once
+#include <cstdint>
+
+#include "sb_ptx.cuh"
+
+namespace sb {
+
+struct WaitCtx {
+    unsigned long long *status;  // (epoch << 32) | code, updated with atomicMax
+    uint32_t epoch;
+    unsigned long long timeout_ns;
+    volatile int *abort_flag;    // in shared memory
+};
+
+constexpr uint32_t kTimeoutStatus = 6;  // SB_ERR_DEVICE_TIMEOUT
+
+__device__ __noinline__ void raise_timeout(const WaitCtx &w) {
+    *w.abort_flag = 1;
+    atomicMax(w.status, (static_cast<unsigned long long>(w.epoch) << 32) | kTimeoutStatus);
+}
+
+// Bounded wait on an mbarrier phase.  Returns false when the CTA is aborting (another role
+// gave up) or when this wait itself runs out of time.
+__device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, const WaitCtx &w) {
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test(bar, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*w.abort_flag) return false;
+            if (globaltimer_ns() - t0 > w.timeout_ns) {
+                raise_timeout(w);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait used while draining: ignores the abort flag (the copies or MMAs being waited
+// for complete on their own), but still gives up after the time limit.
+__device__ __forceinline__ void bwait_drain(uint64_t *bar, uint32_t parity, const WaitCtx &w) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_test(bar, parity)) return;
+        if ((i & 63u) == 63u && globaltimer_ns() - t0 > w.timeout_ns) {
+            raise_timeout(w);
+            return;
+        }
+    }
+}
+
+}  // namespace sb

@@ -72,6 +72,8 @@ def _load():
         lib.oracle_project.restype = ctypes.c_int
         lib.oracle_topk.argtypes = [P, P, i64, i64, i64, i32, P, P, P]
         lib.oracle_topk.restype = ctypes.c_int
+        lib.oracle_partial_completion.argtypes = [P, P, i64, i64, i64, i32, P, P]
+        lib.oracle_partial_completion.restype = ctypes.c_int
         lib.oracle_payload_bytes_per_row.argtypes = [i32, i64]
         lib.oracle_payload_bytes_per_row.restype = f64
         _lib = lib
@@ -144,6 +146,25 @@ def topk(H_bits, W_bits, K: int) -> dict:
                              _ptr(out["logprob"]), _ptr(out["lse"]))
     if rc != 0:
         raise ValueError("oracle_topk rejected its arguments")
+    return out
+
+
+def partial_completion(X_bits, W_bits, lanes: int, keep_partials: bool = False) -> dict:
+    """Row-parallel partial completion (see ``oracle_partial_completion`` in oracle.c):
+    Y [M, N] = sum over lanes of P_l, P_l [M, N] the lane's partial product (fp64)."""
+    X, W = _bits(X_bits), _bits(W_bits)
+    M, K = X.shape
+    N, K2 = W.shape
+    assert K == K2
+    Y = np.empty((M, N))
+    Pp = np.empty((lanes, M, N)) if keep_partials else None
+    rc = _load().oracle_partial_completion(_ptr(X), _ptr(W), M, N, K, int(lanes), _ptr(Y),
+                                           _ptr(Pp))
+    if rc != 0:
+        raise ValueError("oracle_partial_completion rejected its arguments")
+    out = {"Y": Y}
+    if keep_partials:
+        out["P"] = Pp
     return out
 
 

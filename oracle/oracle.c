@@ -286,6 +286,38 @@ int oracle_topk(const uint16_t *H, const uint16_t *W, int64_t M, int64_t d, int6
 }
 
 /*
+ * Partial completion of a row-parallel projection ("SemBridge", Section 6.4 and Table 3: the
+ * MLP down projection is the canonical completion boundary; each tensor-parallel lane owns
+ * a slice of the reduction dimension and produces an incomplete full-width output, and the
+ * partials must be summed before any consumer observes the value; Section 3.5 lists sum
+ * among the registered completion operators).
+ *   X [M][K] activations and W [N][K] weights (bf16 bits); lane l owns reduction columns
+ *   [l*K/lanes, (l+1)*K/lanes).
+ *   P[l][m][n] = sum over lane l's columns i (ascending) of X[m][i] * W[n][i]   (fp64)
+ *   Y[m][n]    = sum over lanes l = 0, 1, ... of P[l][m][n]                    (fp64)
+ * P may be NULL.  Returns 0, or -1 when K is not a multiple of lanes.
+ */
+int oracle_partial_completion(const uint16_t *X, const uint16_t *W, int64_t M, int64_t N,
+                              int64_t K, int32_t lanes, double *Y, double *P) {
+    if (M < 1 || N < 1 || K < 1 || lanes < 1 || K % lanes != 0) return -1;
+    const int64_t Kl = K / lanes;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double y = 0.0;
+            for (int32_t l = 0; l < lanes; ++l) {
+                double part = 0.0;
+                for (int64_t i = l * Kl; i < (l + 1) * Kl; ++i)
+                    part += oracle_bf16_to_double(X[m * K + i]) * oracle_bf16_to_double(W[n * K + i]);
+                if (P) P[(l * M + m) * N + n] = part;
+                y += part;
+            }
+            Y[m * N + n] = y;
+        }
+    return 0;
+}
+
+/*
  * Result bytes a consumer receives per row: the token surface carries one int32
  * ID, the complete-logit surface carries V bf16 logits (the payload contrast of
  * Figure 1 and Figure 3a: k int32 IDs instead of V logit elements).

@@ -32,6 +32,10 @@ MUTATIONS = {
                                    "(best < 0 || zr[j] >= zr[best])"),
     "topk_unnormalised_logprob": ("logprob[r * K + q] = zr[best] - l;",
                                   "logprob[r * K + q] = zr[best];"),
+    "partial_lane_slice_overlaps": ("for (int64_t i = l * Kl; i < (l + 1) * Kl; ++i)",
+                                    "for (int64_t i = l * Kl; i <= (l + 1) * Kl && i < K; ++i)"),
+    "partial_drops_last_lane": ("for (int32_t l = 0; l < lanes; ++l) {",
+                                "for (int32_t l = 0; l + 1 < lanes || l == 0; ++l) {"),
 }
 
 

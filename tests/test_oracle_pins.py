@@ -362,3 +362,39 @@ def test_topk_matches_numpy_stable_argsort():
     assert np.allclose(out["logprob"][:, 0], proj["logprob"], atol=1e-13)
     with pytest.raises(ValueError):
         oracle.topk(Hb, Wb, V + 1)
+
+
+# ---------------------------------------------------------------- partial completion
+@pytest.mark.parametrize("lanes", [1, 2, 4])
+def test_partial_completion_bruteforce(lanes):
+    """Lane partials and their sum against exact rational products (Section 6.4: each lane
+    sums its own slice of the reduction dimension; the completion adds the lanes).
+    Catches a lane slice that overlaps or skips columns and a dropped lane."""
+    M, N, K = 3, 5, 16
+    Xb, Wb = _tiny(M, K, N, seed=44)
+    out = oracle.partial_completion(Xb, Wb, lanes, keep_partials=True)
+    Kl = K // lanes
+    for m in range(M):
+        for n in range(N):
+            parts = [sum(_exact(int(Xb[m, i])) * _exact(int(Wb[n, i]))
+                         for i in range(l * Kl, (l + 1) * Kl)) for l in range(lanes)]
+            for l in range(lanes):
+                assert abs(Fraction(out["P"][l, m, n]) - parts[l]) <= Fraction(1, 2 ** 45)
+            assert abs(Fraction(out["Y"][m, n]) - sum(parts)) <= Fraction(1, 2 ** 44)
+
+
+def test_partial_completion_equals_the_complete_product():
+    """Completing the partials gives the complete product (numpy fp64 matmul, a library
+    routine), and one lane is exactly the complete product's own summation."""
+    M, N, K = 7, 33, 256
+    Xb, Wb = _tiny(M, K, N, seed=45)
+    Xf = (Xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    Wf = (Wb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    ref = Xf @ Wf.T
+    scale = np.abs(Xf) @ np.abs(Wf).T
+    for lanes in (1, 2, 8):
+        Y = oracle.partial_completion(Xb, Wb, lanes)["Y"]
+        assert np.all(np.abs(Y - ref) <= 1e-13 * scale + 1e-300)
+    assert np.array_equal(oracle.partial_completion(Xb, Wb, 1)["Y"], oracle.logits(Xb, Wb))
+    with pytest.raises(ValueError):
+        oracle.partial_completion(Xb, Wb, 3)
