@@ -52,6 +52,10 @@ WORKLOADS = {
                           desc="decode top-8 log-probs: H[16,5120] x W[151936,5120] bf16, k=4"),
     "sampling_token": dict(M=256, d=5120, V=151936, k=4, surface="token_logprob",
                            desc="256-row decode batch: H[256,5120] x W[151936,5120] bf16, k=4, TOKEN + log-prob"),
+    "mlp_down": dict(kind="partial", M=64, N=5120, K=17408, lanes=2,
+                     desc="row-parallel MLP down projection: X[64,17408] x W[5120,17408] bf16, 2 lanes, partials summed, bf16 out"),
+    "mlp_down8": dict(kind="partial", M=8, N=5120, K=17408, lanes=2,
+                      desc="row-parallel MLP down projection, 8 tokens"),
     # smaller cases of the same kernels for ncu captures (inputs still larger than L2)
     "decode16_small": dict(M=16, d=1024, V=151936, k=4, surface="token_logprob",
                            desc="profiling case: H[16,1024] x W[151936,1024] bf16, k=4"),
@@ -243,6 +247,56 @@ def run_reference(args, cfg, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_partial(args, cfg, world, rank, local):
+    """The row-parallel partial completion (lane partials + their ordered sum)."""
+    import torch
+    import gemm_epilogue_reduction_gb300 as sb
+    from gemm_epilogue_reduction_gb300 import build as sbbuild, synth
+    sbbuild.build()
+    torch.cuda.set_device(local)
+    M, N, K, lanes = cfg["M"], cfg["N"], cfg["K"], cfg["lanes"]
+    X, W = synth.make_hw(M, K, N, seed=0, device="cuda")
+    nbytes = sb.sb_partial_workspace_bytes(M, N, K, lanes)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        st = sb.sb_partial_completion(X, W, M, N, K, lanes, Y, True, ws, nbytes, stream)
+        if st != sb.SB_OK:
+            raise sb.SbError(st, "sb_partial_completion")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    K_ = args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        e0.record(stream)
+        for _ in range(K_):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K_
+    peaks, peak_src = load_peaks()
+    alg = N * K * 2 + M * K * 2 + M * N * 2
+    ach = alg / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": M / (ms * 1e-3), "unit": "rows/s", "n_gpus": world,
+        "steps": K_, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "M": M, "N": N, "K": K, "lanes": lanes,
+                   "desc": cfg["desc"], "l2": "W %.0f MB > L2" % (N * K * 2 / 1e6)},
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": f"{peak_src} (HBM copy, burst)",
+                     "kernel": "partial_kernel + complete_kernel", "algorithmic_bytes": alg},
+        "cpu_baseline": None, "e2e": None, "clocks": clocks.summary(), "gpu_launches": 2 * K_,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -260,6 +314,9 @@ def main():
 
     if args.impl == "reference":
         run_reference(args, cfg, world, rank)
+        return
+    if cfg.get("kind") == "partial":
+        run_partial(args, cfg, world, rank, local)
         return
 
     import torch

@@ -81,6 +81,11 @@ def lib():
         L.sb_merge_shard_payload.argtypes = [P, i64, i32, i32, ctypes.c_float,
                                              ctypes.POINTER(sb_outputs), P]
         L.sb_merge_shard_payload.restype = i32
+        L.sb_partial_workspace_bytes.argtypes = [i64, i64, i64, i32]
+        L.sb_partial_workspace_bytes.restype = ctypes.c_size_t
+        L.sb_partial_completion.argtypes = [P, P, i64, i64, i64, i32, P, i32, P,
+                                            ctypes.c_size_t, P]
+        L.sb_partial_completion.restype = i32
         L.sb_last_device_status.argtypes = [ctypes.POINTER(sb_outputs)]
         L.sb_last_device_status.restype = i32
         L.sb_status_string.argtypes = [i32]
@@ -165,6 +170,36 @@ def sb_merge_shard_payload(payload, M, k, surface, temperature, out: sb_outputs,
                            stream=None) -> int:
     return int(lib().sb_merge_shard_payload(_ptr(payload), M, k, surface, float(temperature),
                                             ctypes.byref(out), _stream(stream)))
+
+
+def sb_partial_workspace_bytes(M: int, N: int, K: int, lanes: int) -> int:
+    return int(lib().sb_partial_workspace_bytes(M, N, K, lanes))
+
+
+def sb_partial_completion(X, W, M, N, K, lanes, Y, y_bf16, workspace, workspace_bytes,
+                          stream=None) -> int:
+    return int(lib().sb_partial_completion(_ptr(X), _ptr(W), M, N, K, lanes, _ptr(Y),
+                                           1 if y_bf16 else 0, _ptr(workspace),
+                                           int(workspace_bytes), _stream(stream)))
+
+
+def partial_completion(X, W, lanes: int, *, out_bf16: bool = True, stream=None, workspace=None):
+    """Y = sum over lanes of X[:, lane] W[:, lane]^T for torch CUDA bf16 tensors X [M, K] and
+    W [N, K]; returns (Y, workspace).  Raises SbError on a bad status."""
+    import torch
+    M, K = X.shape
+    N = W.shape[0]
+    nbytes = sb_partial_workspace_bytes(M, N, K, lanes)
+    if nbytes == 0:
+        raise SbError(SB_ERR_INVALID_ARG, "sb_partial_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=X.device)
+    Y = torch.empty(M, N, dtype=torch.bfloat16 if out_bf16 else torch.float32, device=X.device)
+    st = sb_partial_completion(X, W, M, N, K, lanes, Y, out_bf16, workspace,
+                               workspace.numel(), stream)
+    if st != SB_OK:
+        raise SbError(st, "sb_partial_completion")
+    return Y, workspace
 
 
 def sb_last_device_status(out: sb_outputs) -> int:

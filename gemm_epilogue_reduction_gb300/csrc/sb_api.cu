@@ -239,6 +239,22 @@ CombineParams combine_params(const sb_outputs *out, const Workspace &w, int64_t 
 
 }  // namespace
 
+namespace sb {
+bool encode_bf16_map(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols,
+                     int box_rows) {
+    return make_map(tm, base, rows, cols, box_rows);
+}
+int32_t device_sms_cc(int *sms, int *cc) {
+    DevInfo dev;
+    const int32_t e = current_device(&dev);
+    if (sms) *sms = dev.sms;
+    if (cc) *cc = dev.cc;
+    return e;
+}
+uint32_t next_epoch() { return g_epoch.fetch_add(1) + 1; }
+unsigned long long wait_limit_ns() { return g_timeout_ns.load(); }
+}  // namespace sb
+
 extern "C" {
 
 size_t sb_workspace_bytes(int64_t M, int64_t V, int32_t k, int32_t surface) {

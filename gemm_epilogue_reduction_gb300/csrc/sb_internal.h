@@ -98,4 +98,11 @@ cudaError_t launch_merge_payload(const CombineParams &c, const void *payload,
 
 size_t lmhead_smem_bytes(int nb, int stages_a, int stages_b, bool vocab_mode, int flags);
 
+// Host helpers shared by the entry points (sb_api.cu).
+bool encode_bf16_map(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols,
+                     int box_rows);
+int32_t device_sms_cc(int *sms, int *cc);  // SB_OK, SB_ERR_CUDA or SB_ERR_UNSUPPORTED
+uint32_t next_epoch();
+unsigned long long wait_limit_ns();
+
 }  // namespace sb

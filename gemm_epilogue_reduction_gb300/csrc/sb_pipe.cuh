@@ -19,7 +19,7 @@ struct WaitCtx {
 
 constexpr uint32_t kTimeoutStatus = 6;  // SB_ERR_DEVICE_TIMEOUT
 
-__device__ __noinline__ void raise_timeout(const WaitCtx &w) {
+static __device__ __noinline__ void raise_timeout(const WaitCtx &w) {
     *w.abort_flag = 1;
     atomicMax(w.status, (static_cast<unsigned long long>(w.epoch) << 32) | kTimeoutStatus);
 }

@@ -248,6 +248,30 @@ int32_t sb_pack_shard_records(const void *workspace, int64_t M, int32_t k,
 int32_t sb_merge_shard_payload(const void *payload, int64_t M, int32_t k, int32_t surface,
                                float temperature, const sb_outputs *out, void *stream);
 
+/*
+ * Row-parallel partial completion ("SemBridge", Section 6.4 and Table 3: in a row-parallel
+ * MLP down projection each tensor-parallel lane owns a slice of the reduction dimension and
+ * produces an incomplete full-width partial; the partials must be summed -- the completion
+ * obligation of Section 3.5 -- before a consumer observes the value).
+ *   Y[m][n] = sum over lanes l (ascending) of P_l[m][n],
+ *   P_l[m][n] = sum over lane l's reduction columns of X[m][i] * W[n][i].
+ *   X          device bf16 [M, K] row-major (activations), 16-byte aligned; 1 <= M <= 256.
+ *   W          device bf16 [N, K] row-major (weights), 16-byte aligned; N >= 1.
+ *   K          a multiple of 64 * lanes (each lane's slice is whole 64-column blocks).
+ *   lanes      >= 1.
+ *   Y          device [M, N] row-major: fp32 when y_bf16 == 0, else bf16 (round to nearest).
+ *   workspace  device, 256-byte aligned, >= sb_partial_workspace_bytes(M, N, K, lanes):
+ *              header (read by sb_last_device_status) + fp32 partials; no initialisation.
+ * Each lane's slice is cut into equal chunks so the work fills the GPU; the partials are
+ * accumulated in fp32 on the tensor cores and summed in ascending chunk order (lane 0's
+ * chunks first), so the result bits do not depend on scheduling.  Two kernels are enqueued
+ * on stream; returns SB_OK or an error with nothing enqueued.
+ */
+size_t sb_partial_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t lanes);
+int32_t sb_partial_completion(const void *X, const void *W, int64_t M, int64_t N, int64_t K,
+                              int32_t lanes, void *Y, int32_t y_bf16, void *workspace,
+                              size_t workspace_bytes, void *stream);
+
 /* Device status of the last call that used out->workspace: SB_OK or
  * SB_ERR_DEVICE_TIMEOUT.  Synchronous: copies the header to the host (call it after
  * synchronising the stream).  Returns SB_ERR_CUDA if the copy fails. */
