@@ -739,16 +739,18 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmP
     // persistent grid: as many clusters as can be resident at once (one CTA per SM)
     int clusters = num_sms / CS;
     if (CS > 1) {
-        // co-resident clusters (GPCs may not pair every SM); queried once per device for the
-        // largest shared-memory footprint this kernel is launched with
-        static std::atomic<int> active_by_dev[64];
-        int active = (dev < 64) ? active_by_dev[dev].load() : 0;
+        // co-resident clusters (GPCs may not pair every SM), queried for this launch's
+        // shared-memory footprint and cached per device for the last footprint asked
+        static std::atomic<unsigned long long> cache_by_dev[64];  // (smem << 32) | active
+        const unsigned long long c = dev < 64 ? cache_by_dev[dev].load() : 0;
+        int active = (c >> 32) == smem ? static_cast<int>(c & 0xFFFFFFFFu) : 0;
         if (active <= 0) {
             cudaLaunchConfig_t q = cfg;
             q.gridDim = dim3(CS * clusters);
-            q.dynamicSmemBytes = kSmemLimit;
             if (cudaOccupancyMaxActiveClusters(&active, kern, &q) != cudaSuccess) active = 0;
-            if (active > 0 && dev < 64) active_by_dev[dev].store(active);
+            if (active > 0 && dev < 64)
+                cache_by_dev[dev].store((static_cast<unsigned long long>(smem) << 32) |
+                                        static_cast<unsigned>(active));
         }
         if (active > 0) clusters = active < clusters ? active : clusters;
     }

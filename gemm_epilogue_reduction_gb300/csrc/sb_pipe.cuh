@@ -19,14 +19,17 @@ struct WaitCtx {
 
 constexpr uint32_t kTimeoutStatus = 6;  // SB_ERR_DEVICE_TIMEOUT
 
-static __device__ __noinline__ void raise_timeout(const WaitCtx &w) {
-    *w.abort_flag = 1;
-    atomicMax(w.status, (static_cast<unsigned long long>(w.epoch) << 32) | kTimeoutStatus);
+// Scalars by value: a context passed by reference to an out-of-line function would be kept
+// in local memory at every wait site.
+static __device__ __noinline__ void raise_timeout(unsigned long long *status, uint32_t epoch,
+                                                  volatile int *abort_flag) {
+    *abort_flag = 1;
+    atomicMax(status, (static_cast<unsigned long long>(epoch) << 32) | kTimeoutStatus);
 }
 
 // Bounded wait on an mbarrier phase.  Returns false when the CTA is aborting (another role
 // gave up) or when this wait itself runs out of time.
-__device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, const WaitCtx &w) {
+__device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, const WaitCtx w) {
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
@@ -34,7 +37,7 @@ __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, const Wait
         if ((i & 63u) == 0) {
             if (*w.abort_flag) return false;
             if (globaltimer_ns() - t0 > w.timeout_ns) {
-                raise_timeout(w);
+                raise_timeout(w.status, w.epoch, w.abort_flag);
                 return false;
             }
         }
@@ -43,12 +46,12 @@ __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, const Wait
 
 // Bounded wait used while draining: ignores the abort flag (the copies or MMAs being waited
 // for complete on their own), but still gives up after the time limit.
-__device__ __forceinline__ void bwait_drain(uint64_t *bar, uint32_t parity, const WaitCtx &w) {
+__device__ __forceinline__ void bwait_drain(uint64_t *bar, uint32_t parity, const WaitCtx w) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 0;; ++i) {
         if (mbar_test(bar, parity)) return;
         if ((i & 63u) == 63u && globaltimer_ns() - t0 > w.timeout_ns) {
-            raise_timeout(w);
+            raise_timeout(w.status, w.epoch, w.abort_flag);
             return;
         }
     }
