@@ -140,6 +140,14 @@ __device__ __forceinline__ uint32_t uniform_bits24(unsigned long long seed, unsi
     return static_cast<uint32_t>(x >> 40);
 }
 
+__device__ __forceinline__ uint32_t select_u32(bool pred, uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\tselp.b32 %0, %2, %3, p;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(a), "r"(b));
+    return r;
+}
+
 __device__ __forceinline__ uint16_t bf16_bits_rn(float z) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(z));
 }
@@ -434,11 +442,13 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
             }
         }
         if (tgt >= cb && tgt < cb + nval) {
-            float tzv = 0.f;
+            // an explicit select chain: written as "pick raw[tgt - cb]" the compiler moves
+            // raw[] to local memory to index it
+            uint32_t tzv = 0u;
+            const int off = tgt - cb;
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (j == tgt - cb) tzv = __uint_as_float(raw[j]);
-            p.ws.tz[row] = tzv;
+            for (int j = 0; j < 32; ++j) tzv = select_u32(j == off, raw[j], tzv);
+            p.ws.tz[row] = __uint_as_float(tzv);
         }
         if (FULL && rv) {
             uint16_t *dst = p.logits + static_cast<size_t>(row) * p.V + cb;
