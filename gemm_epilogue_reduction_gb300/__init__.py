@@ -86,6 +86,9 @@ def lib():
         L.sb_partial_completion.argtypes = [P, P, i64, i64, i64, i32, P, i32, P,
                                             ctypes.c_size_t, P]
         L.sb_partial_completion.restype = i32
+        L.sb_select_source_projection.argtypes = [ctypes.c_double] * 8 + [
+            ctypes.POINTER(ctypes.c_double)]
+        L.sb_select_source_projection.restype = i32
         L.sb_last_device_status.argtypes = [ctypes.POINTER(sb_outputs)]
         L.sb_last_device_status.restype = i32
         L.sb_status_string.argtypes = [i32]
@@ -200,6 +203,18 @@ def partial_completion(X, W, lanes: int, *, out_bf16: bool = True, stream=None, 
     if st != SB_OK:
         raise SbError(st, "sb_partial_completion")
     return Y, workspace
+
+
+def sb_select_source_projection(bytes_ref, bytes_proj, frames_ref, frames_proj,
+                                link_bytes_per_s, frame_startup_s, local_proj_s, local_ref_s):
+    """Equation (7) plan choice: returns (decision, margin_s); 1 = project at the source."""
+    m = ctypes.c_double(0.0)
+    d = lib().sb_select_source_projection(float(bytes_ref), float(bytes_proj),
+                                          float(frames_ref), float(frames_proj),
+                                          float(link_bytes_per_s), float(frame_startup_s),
+                                          float(local_proj_s), float(local_ref_s),
+                                          ctypes.byref(m))
+    return int(d), float(m.value)
 
 
 def sb_last_device_status(out: sb_outputs) -> int:

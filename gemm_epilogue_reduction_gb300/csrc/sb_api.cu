@@ -438,6 +438,23 @@ int32_t sb_merge_shard_payload(const void *payload, int64_t M, int32_t k, int32_
     return SB_OK;
 }
 
+int32_t sb_select_source_projection(double bytes_ref, double bytes_proj, double frames_ref,
+                                    double frames_proj, double link_bytes_per_s,
+                                    double frame_startup_s, double local_proj_s,
+                                    double local_ref_s, double *margin_s) {
+    const double in[] = {bytes_ref, bytes_proj, frames_ref, frames_proj, frame_startup_s};
+    for (double v : in)
+        if (!(v >= 0.0) || !std::isfinite(v)) return -1;
+    if (!(link_bytes_per_s > 0.0) || !std::isfinite(link_bytes_per_s) ||
+        !std::isfinite(local_proj_s) || !std::isfinite(local_ref_s))
+        return -1;
+    const double saved = (bytes_ref - bytes_proj) / link_bytes_per_s +
+                         frame_startup_s * (frames_ref - frames_proj);
+    const double added = local_proj_s - local_ref_s;
+    if (margin_s) *margin_s = saved - added;
+    return saved > added ? 1 : 0;
+}
+
 int32_t sb_last_device_status(const sb_outputs *out) {
     if (!out || !out->workspace || out->workspace_bytes < 16) return SB_ERR_INVALID_ARG;
     uint64_t hdr[2] = {0, 0};

@@ -272,6 +272,23 @@ int32_t sb_partial_completion(const void *X, const void *W, int64_t M, int64_t N
                               int32_t lanes, void *Y, int32_t y_bf16, void *workspace,
                               size_t workspace_bytes, void *stream);
 
+/*
+ * The decision before the path ("SemBridge", Section 8.2, Equation (7)): between the
+ * checker-accepted plans, project at the source (plan s) rather than transfer the complete
+ * logits (plan r) when the transfer saved exceeds the local cost added:
+ *   (bytes_ref - bytes_proj) / link_bytes_per_s + frame_startup_s * (frames_ref - frames_proj)
+ *       > local_proj_s - local_ref_s.
+ * Bytes and frames are those crossing the link per step; the local costs are the two plans'
+ * on-device times (for example this library's sb_lmhead_project time for the projected
+ * surface and for SB_FULL_LOGITS).  *margin_s (may be NULL) receives left minus right side.
+ * Returns 1 (project), 0 (transfer complete logits), or -1 for a non-positive or non-finite
+ * bandwidth or a negative or non-finite byte, frame or startup argument.  Host only.
+ */
+int32_t sb_select_source_projection(double bytes_ref, double bytes_proj, double frames_ref,
+                                    double frames_proj, double link_bytes_per_s,
+                                    double frame_startup_s, double local_proj_s,
+                                    double local_ref_s, double *margin_s);
+
 /* Device status of the last call that used out->workspace: SB_OK or
  * SB_ERR_DEVICE_TIMEOUT.  Synchronous: copies the header to the host (call it after
  * synchronising the stream).  Returns SB_ERR_CUDA if the copy fails. */

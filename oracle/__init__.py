@@ -74,6 +74,8 @@ def _load():
         lib.oracle_topk.restype = ctypes.c_int
         lib.oracle_partial_completion.argtypes = [P, P, i64, i64, i64, i32, P, P]
         lib.oracle_partial_completion.restype = ctypes.c_int
+        lib.oracle_select_source_projection.argtypes = [f64] * 8 + [P]
+        lib.oracle_select_source_projection.restype = ctypes.c_int
         lib.oracle_payload_bytes_per_row.argtypes = [i32, i64]
         lib.oracle_payload_bytes_per_row.restype = f64
         _lib = lib
@@ -147,6 +149,15 @@ def topk(H_bits, W_bits, K: int) -> dict:
     if rc != 0:
         raise ValueError("oracle_topk rejected its arguments")
     return out
+
+
+def select_source_projection(B_r, B_s, F_r, F_s, beta, alpha, L_s, L_r):
+    """Equation (7): (decision, margin in seconds); decision 1 = project, 0 = materialise."""
+    m = ctypes.c_double(0.0)
+    d = _load().oracle_select_source_projection(float(B_r), float(B_s), float(F_r), float(F_s),
+                                                float(beta), float(alpha), float(L_s),
+                                                float(L_r), ctypes.byref(m))
+    return int(d), float(m.value)
 
 
 def partial_completion(X_bits, W_bits, lanes: int, keep_partials: bool = False) -> dict:

@@ -318,6 +318,30 @@ int oracle_partial_completion(const uint16_t *X, const uint16_t *W, int64_t M, i
 }
 
 /*
+ * Fabric-aware selection between checker-accepted plans, Equation (7) of Section 8.2: the
+ * specialised plan s (source projection) is preferred over the reference plan r
+ * (complete-logit transfer) when the transfer it saves exceeds the local cost it adds,
+ *   (B_r - B_s) / beta + alpha * (F_r - F_s) > L_s - L_r,
+ * with B the remote bytes, F the remote frames (startups), beta the link bandwidth in
+ * bytes per second, alpha the cost of one frame startup in seconds, and L the local cost
+ * (projection and native collectives) in seconds.  *margin (if not NULL) receives the left
+ * side minus the right side.  Returns 1 (project at the source), 0 (transfer the complete
+ * logits) or -1 for a non-positive or non-finite bandwidth or a negative or non-finite
+ * byte, frame or startup input.
+ */
+int oracle_select_source_projection(double B_r, double B_s, double F_r, double F_s, double beta,
+                                    double alpha, double L_s, double L_r, double *margin) {
+    if (!(beta > 0.0) || !isfinite(beta) || !(B_r >= 0.0) || !(B_s >= 0.0) || !(F_r >= 0.0) ||
+        !(F_s >= 0.0) || !(alpha >= 0.0) || !isfinite(B_r) || !isfinite(B_s) || !isfinite(F_r) ||
+        !isfinite(F_s) || !isfinite(alpha) || !isfinite(L_s) || !isfinite(L_r))
+        return -1;
+    const double lhs = (B_r - B_s) / beta + alpha * (F_r - F_s);
+    const double rhs = L_s - L_r;
+    if (margin) *margin = lhs - rhs;
+    return lhs > rhs ? 1 : 0;
+}
+
+/*
  * Result bytes a consumer receives per row: the token surface carries one int32
  * ID, the complete-logit surface carries V bf16 logits (the payload contrast of
  * Figure 1 and Figure 3a: k int32 IDs instead of V logit elements).

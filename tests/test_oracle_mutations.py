@@ -34,6 +34,8 @@ MUTATIONS = {
                                   "logprob[r * K + q] = zr[best];"),
     "partial_lane_slice_overlaps": ("for (int64_t i = l * Kl; i < (l + 1) * Kl; ++i)",
                                     "for (int64_t i = l * Kl; i <= (l + 1) * Kl && i < K; ++i)"),
+    "selection_local_cost_sign": ("const double rhs = L_s - L_r;", "const double rhs = L_r - L_s;"),
+    "selection_frames_ignored": ("+ alpha * (F_r - F_s);", "+ 0.0 * alpha * (F_r - F_s);"),
     "partial_drops_last_lane": ("for (int32_t l = 0; l < lanes; ++l) {",
                                 "for (int32_t l = 0; l + 1 < lanes || l == 0; ++l) {"),
 }

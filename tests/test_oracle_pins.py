@@ -398,3 +398,36 @@ def test_partial_completion_equals_the_complete_product():
     assert np.array_equal(oracle.partial_completion(Xb, Wb, 1)["Y"], oracle.logits(Xb, Wb))
     with pytest.raises(ValueError):
         oracle.partial_completion(Xb, Wb, 3)
+
+
+# ---------------------------------------------------------------- Eq. (7) selection
+def _fig2():
+    return {r[0]: float(r[1]) for r in _read_golden("fig2_result_path.txt")}
+
+
+def test_selection_reproduces_the_pages_choice_on_their_testbed():
+    """With Figure 2's bytes and frames, the 1-GbE link of Section 6.1 and the 0.189 ms
+    projection cost, Equation (7) picks source projection, as the deployment did; the saving
+    is the logit bytes' wire time (~25.6 ms)."""
+    g = _fig2()
+    beta = g["link_bits_per_s"] / 8.0
+    d, margin = oracle.select_source_projection(g["r0_bytes"], g["p0_bytes"], g["r0_frames"],
+                                                g["p0_frames"], beta, g["rtt"],
+                                                g["projection_cost"], 0.0)
+    assert d == g["chosen_plan"]
+    assert abs(margin - ((3201544 - 256) / beta - 0.189e-3)) < 1e-12
+
+
+def test_selection_flips_when_the_local_cost_exceeds_the_transfer_saved():
+    """A link fast enough that the bytes saved take less time than the projection costs
+    (closed form: threshold bandwidth = (B_r - B_s) / (L_s - L_r)), and the frame term."""
+    g = _fig2()
+    dB = g["r0_bytes"] - g["p0_bytes"]
+    L = g["projection_cost"]
+    thr = dB / L
+    assert oracle.select_source_projection(dB + 256, 256, 4, 4, thr * 0.99, 0.0, L, 0.0)[0] == 1
+    assert oracle.select_source_projection(dB + 256, 256, 4, 4, thr * 1.01, 0.0, L, 0.0)[0] == 0
+    # fewer frames on the projected plan add alpha per frame saved
+    d, m = oracle.select_source_projection(1000, 1000, 5, 1, 1e9, 1e-3, 3.5e-3, 0.0)
+    assert d == 1 and abs(m - 0.5e-3) < 1e-15
+    assert oracle.select_source_projection(1, 0, 1, 1, 0.0, 0.0, 0.0, 0.0)[0] == -1
