@@ -56,6 +56,8 @@ WORKLOADS = {
                      desc="row-parallel MLP down projection: X[64,17408] x W[5120,17408] bf16, 2 lanes, partials summed, bf16 out"),
     "mlp_down8": dict(kind="partial", M=8, N=5120, K=17408, lanes=2,
                       desc="row-parallel MLP down projection, 8 tokens"),
+    "mlp_down_small": dict(kind="partial", M=64, N=2048, K=17408, lanes=2,
+                           desc="profiling case: X[64,17408] x W[2048,17408] bf16, 2 lanes"),
     # smaller cases of the same kernels for ncu captures (inputs still larger than L2)
     "decode16_small": dict(M=16, d=1024, V=151936, k=4, surface="token_logprob",
                            desc="profiling case: H[16,1024] x W[151936,1024] bf16, k=4"),
@@ -73,8 +75,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # null once the source differs.
 KERNEL_TRAFFIC = {
     # decode16: dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
-    # (1,556,163,072 + 3,185,664 B; W + H are 1,555,988,480 B).
-    "decode16": {"bytes": 1559348736, "src_sha": "29e05b26d955f669"},
+    # (1,556,177,664 + 3,352,576 B; W + H are 1,555,988,480 B).
+    "decode16": {"bytes": 1559530240, "src_sha": "1d906b56533447fb"},
 }
 
 
