@@ -178,3 +178,27 @@ def test_gumbel_noise_transform_exhaustive_over_all_24bit_uniforms():
     assert got[0] == -math.inf and np.isfinite(got[1:]).all()
     err = np.abs(got[1:] - want[1:])
     assert err.max() <= 2e-6, (float(err.max()), int(err.argmax()) + 1)
+
+
+@pytest.mark.parametrize("M,d,V,k", [
+    (3, 8, 1, 1),         # one column: token 0, log-prob 0, lse = z
+    (5, 64, 3072, 1024),  # the largest shard count (S = 3)
+    (200, 8, 1000, 2),    # rows mode with the smallest d
+    (1, 8, 7, 7),         # one row, one column per shard
+])
+def test_degenerate_and_extreme_shapes(M, d, V, k):
+    res, ref, _ = run_and_check(M, d, V, k, sb.SB_TOKEN_LOGPROB, seed=M * 7 + V, targets=True)
+    if V == 1:
+        assert res["token"].tolist() == [0] * M
+        assert torch.allclose(res["token_logprob"], torch.zeros_like(res["token_logprob"]))
+
+
+def test_topk_at_its_limits():
+    """K = 16 with k = 128 lanes (the top-K limits)."""
+    from test_topk import check_topk
+    M, d, V, k, K = 4, 64, 128 * 20, 128, 16
+    H, W = synth.make_hw(M, d, V, seed=77)
+    H, W = H.cuda(), W.cuda()
+    res = sb.project(H, W, k, sb.SB_TOPK_LOGPROB, topk=K)
+    torch.cuda.synchronize()
+    check_topk(res, H, W, K)
