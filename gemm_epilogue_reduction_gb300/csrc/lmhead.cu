@@ -597,6 +597,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (VOCAB && (p.flags & kFlagTargets))
         for (int i = threadIdx.x; i < p.M; i += blockDim.x) tgt_s[i] = p.targets[i];
+    // Scoring targets outside [0, V) would leave their log-prob undefined: CTA 0 checks them
+    // and reports SB_ERR_INVALID_ARG through the status word (the outputs stay undefined).
+    if (blockIdx.x == 0 && (p.flags & kFlagTargets)) {
+        bool bad = false;
+        for (int i = threadIdx.x; i < p.M; i += blockDim.x) {
+            const int t = p.targets[i];
+            bad |= (t < 0 || t >= p.V);
+        }
+        if (bad) atomicMax(p.ws.status, (static_cast<unsigned long long>(p.epoch) << 32) | 1ull);
+    }
     if (warp == 1) {
         tmem_alloc(tmem_slot, tmem_cols);
         tmem_relinquish();

@@ -462,8 +462,10 @@ int32_t sb_last_device_status(const sb_outputs *out) {
         return SB_ERR_CUDA;
     const uint32_t epoch = static_cast<uint32_t>(hdr[0] & 0xFFFFFFFFu);
     const uint64_t st = hdr[1];
-    if (static_cast<uint32_t>(st >> 32) == epoch && static_cast<uint32_t>(st) == SB_ERR_DEVICE_TIMEOUT)
-        return SB_ERR_DEVICE_TIMEOUT;
+    const uint32_t code = static_cast<uint32_t>(st);
+    if (static_cast<uint32_t>(st >> 32) == epoch &&
+        (code == SB_ERR_DEVICE_TIMEOUT || code == SB_ERR_INVALID_ARG))
+        return static_cast<int32_t>(code);
     return SB_OK;
 }
 

@@ -77,7 +77,9 @@ typedef enum sb_status {
  *                                  [s*V/k, (s+1)*V/k)); required iff SB_FULL_LOGITS and
  *                                  written only then.
  *   target_ids      int32 [M]      optional scoring targets, each in [0, V).  Values out of
- *                                  range are not detected and give an undefined result.
+ *                                  range are found on the device: sb_last_device_status
+ *                                  then reports SB_ERR_INVALID_ARG and the outputs are
+ *                                  undefined.
  *   target_logprob  float [M]      log p(target_ids[r]); required iff target_ids != NULL.
  *   workspace       bytes          scratch of at least sb_workspace_bytes(M, V, k, surface)
  *                                  bytes, 256-byte aligned; holds the per-tile records, the
@@ -289,9 +291,10 @@ int32_t sb_select_source_projection(double bytes_ref, double bytes_proj, double 
                                     double frame_startup_s, double local_proj_s,
                                     double local_ref_s, double *margin_s);
 
-/* Device status of the last call that used out->workspace: SB_OK or
- * SB_ERR_DEVICE_TIMEOUT.  Synchronous: copies the header to the host (call it after
- * synchronising the stream).  Returns SB_ERR_CUDA if the copy fails. */
+/* Device status of the last call that used out->workspace: SB_OK, SB_ERR_DEVICE_TIMEOUT
+ * (a bounded wait gave up) or SB_ERR_INVALID_ARG (a scoring target outside [0, V); when
+ * both happen the timeout is reported).  Synchronous: copies the header to the host (call
+ * it after synchronising the stream).  Returns SB_ERR_CUDA if the copy fails. */
 int32_t sb_last_device_status(const sb_outputs *out);
 
 /* Static description of a status code; never NULL. */

@@ -202,3 +202,25 @@ def test_topk_at_its_limits():
     res = sb.project(H, W, k, sb.SB_TOPK_LOGPROB, topk=K)
     torch.cuda.synchronize()
     check_topk(res, H, W, K)
+
+
+@pytest.mark.parametrize("M", [16, 300])
+def test_out_of_range_targets_are_reported_on_the_device(M):
+    """A scoring target outside [0, V) is caught by the kernel and reported through the
+    status word; the next call with valid targets is clean."""
+    d, V, k = 64, 1000, 2
+    H, W = synth.make_hw(M, d, V, seed=4)
+    H, W = H.cuda(), W.cuda()
+    tg = synth.make_targets(M, V, device="cuda")
+    bad = tg.clone()
+    bad[M // 2] = V
+    res = sb.project(H, W, k, sb.SB_TOKEN_LOGPROB, targets=bad)
+    torch.cuda.synchronize()
+    assert sb.sb_last_device_status(res["_outputs"]) == sb.SB_ERR_INVALID_ARG
+    bad[M // 2] = -3
+    res = sb.project(H, W, k, sb.SB_TOKEN_LOGPROB, targets=bad, workspace=res["workspace"])
+    torch.cuda.synchronize()
+    assert sb.sb_last_device_status(res["_outputs"]) == sb.SB_ERR_INVALID_ARG
+    res = sb.project(H, W, k, sb.SB_TOKEN_LOGPROB, targets=tg, workspace=res["workspace"])
+    torch.cuda.synchronize()
+    assert sb.sb_last_device_status(res["_outputs"]) == sb.SB_OK
