@@ -405,10 +405,14 @@ def main():
     comb_ms = [evk[2 * i].elapsed_time(evk[2 * i + 1]) for i in range(K)]
 
     # ---- end to end through the public call, host buffers
+    # token and log-prob live side by side in one device buffer, read back with one copy
     E = min(args.e2e_steps, K)
     H_host = H.cpu().pin_memory()
-    tok_host = torch.empty(M, dtype=torch.int32).pin_memory()
-    lp_host = torch.empty(M, dtype=torch.float32).pin_memory()
+    res_dev = torch.empty(2 * M, dtype=torch.int32, device="cuda")
+    res_host = torch.empty(2 * M, dtype=torch.int32).pin_memory()
+    e2e_out = sb.sb_outputs(res_dev.data_ptr(), res_dev.data_ptr() + 4 * M, out.lse,
+                            out.logits_bf16, out.target_ids, out.target_logprob, out.workspace,
+                            out.workspace_bytes, out.topk_ids, out.topk_logprob, out.topk)
     H_dev = torch.empty_like(H)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -416,11 +420,10 @@ def main():
     e0.record(stream)
     for _ in range(E):
         H_dev.copy_(H_host, non_blocking=True)
-        st = sb.sb_lmhead_project(H_dev, W, M, d, V, k, surface, T, gseed, out, stream)
+        st = sb.sb_lmhead_project(H_dev, W, M, d, V, k, surface, T, gseed, e2e_out, stream)
         if st != sb.SB_OK:
             raise sb.SbError(st, "sb_lmhead_project")
-        tok_host.copy_(bufs["token"], non_blocking=True)
-        lp_host.copy_(bufs["token_logprob"], non_blocking=True)
+        res_host.copy_(res_dev, non_blocking=True)
         stream.synchronize()
     e1.record(stream)
     torch.cuda.synchronize()

@@ -224,3 +224,29 @@ def test_out_of_range_targets_are_reported_on_the_device(M):
     res = sb.project(H, W, k, sb.SB_TOKEN_LOGPROB, targets=tg, workspace=res["workspace"])
     torch.cuda.synchronize()
     assert sb.sb_last_device_status(res["_outputs"]) == sb.SB_OK
+
+
+def test_gpu_gumbel_sampler_draws_from_the_tempered_softmax():
+    """20,000 rows share one hidden state, so every row is an independent draw from the same
+    softmax(z / T) (the noise index is row * V + column): the GPU token frequencies pass a
+    chi-square test against it, and each row's token matches the oracle's draw wherever the
+    oracle's top-2 key gap exceeds 1e-2."""
+    d, V, T, N = 8, 6, 0.7, 20000
+    zvals = [0.0, 0.5, 1.0, 1.5, -1.0, 2.0]  # exactly representable in bf16
+    W = torch.zeros(V, d, dtype=torch.bfloat16)
+    W[:, 0] = torch.tensor(zvals, dtype=torch.bfloat16)
+    H = torch.zeros(N, d, dtype=torch.bfloat16)
+    H[:, 0] = 1.0
+    res = sb.project(H.cuda(), W.cuda(), 2, sb.SB_GUMBEL_TOKEN, temperature=T, seed=4321)
+    torch.cuda.synchronize()
+    tok = res["token"].cpu().numpy()
+    counts = np.bincount(tok, minlength=V).astype(float)
+    p = np.exp(np.array(zvals) / np.float32(T))
+    p /= p.sum()
+    chi2 = ((counts - N * p) ** 2 / (N * p)).sum()
+    assert chi2 < 30.0  # 5 degrees of freedom: p < 2e-5 above this
+    ref = oracle.project(synth.bf16_bits(H), synth.bf16_bits(W), 2, gumbel=True,
+                         temperature=np.float32(T).item(), seed=4321)
+    sure = (ref["key_top1"] - ref["key_top2"]) > 1e-2
+    assert np.array_equal(tok[sure], ref["token"][sure])
+    assert sure.mean() > 0.99
