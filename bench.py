@@ -47,6 +47,9 @@ WORKLOADS = {
                     desc="prefill scoring: H[4096,6144] x W[200064,6144] bf16, k=4, lse + target log-prob"),
     "sampling": dict(M=256, d=5120, V=151936, k=4, surface="gumbel_token", T=0.7, seed=1234,
                      desc="seeded sampling: H[256,5120] x W[151936,5120] bf16, k=4, GUMBEL_TOKEN T=0.7"),
+    "decode16_sample": dict(M=16, d=5120, V=151936, k=4, surface="gumbel_token", T=0.7,
+                            seed=1234,
+                            desc="decode seeded sampling: H[16,5120] x W[151936,5120] bf16, k=4, GUMBEL_TOKEN T=0.7"),
     "tiny": dict(M=4, d=256, V=4096, k=2, surface="token_logprob",
                  desc="tiny: H[4,256] x W[4096,256] bf16, k=2"),
     "decode16_topk": dict(M=16, d=5120, V=151936, k=4, surface="topk_logprob", topk=8,
@@ -64,6 +67,8 @@ WORKLOADS = {
                            desc="profiling case: H[16,1024] x W[151936,1024] bf16, k=4"),
     "prefill_small": dict(M=1024, d=2048, V=65536, k=4, surface="token_logprob", targets=True,
                           desc="profiling case: H[1024,2048] x W[65536,2048] bf16, k=4"),
+    "sampling_token_small": dict(M=256, d=5120, V=65536, k=4, surface="token_logprob",
+                                 desc="profiling case: H[256,5120] x W[65536,5120] bf16, k=4"),
     "sampling_small": dict(M=256, d=1024, V=151936, k=4, surface="gumbel_token", T=0.7,
                            seed=1234,
                            desc="profiling case: H[256,1024] x W[151936,1024] bf16, k=4, GUMBEL"),

@@ -130,13 +130,18 @@ __device__ __forceinline__ bool epi_vote_any(bool pred) {
 }
 
 // Counter-based uniform: SplitMix64 (Steele, Lea and Flood, OOPSLA 2014) at stream index n
-// of the stream seeded with `seed` (state seed + (n + 1) * golden-ratio increment, then the
-// finaliser); the top 24 bits b give u = b * 2^-24 in [0, 1).
-__device__ __forceinline__ uint32_t uniform_bits24(unsigned long long seed, unsigned long long n) {
-    unsigned long long x = seed + (n + 1ull) * 0x9E3779B97F4A7C15ull;
+// of the stream seeded with `seed`: the state is seed + (n + 1) * golden-ratio increment,
+// then the finaliser; the top 24 bits b give u = b * 2^-24 in [0, 1).
+constexpr unsigned long long kGolden = 0x9E3779B97F4A7C15ull;
+__device__ __forceinline__ unsigned long long splitmix_state(unsigned long long seed,
+                                                             unsigned long long n) {
+    return seed + (n + 1ull) * kGolden;
+}
+// The finaliser ends with x ^= x >> 31; its top 24 bits are those of x itself (x >> 31
+// contributes nothing above bit 32), so that last step is left out.
+__device__ __forceinline__ uint32_t bits24_from_state(unsigned long long x) {
     x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
     x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
-    x ^= x >> 31;
     return static_cast<uint32_t>(x >> 40);
 }
 
@@ -189,6 +194,13 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
             tmem_ld32x32b_x16(taddr + c0, raw);
         float my_m = -INFINITY, my_s = 0.f, my_gk = -INFINITY, my_gz = 0.f;
         int my_i = INT_MAX, my_gi = INT_MAX;
+        // stream index of (row c0 + j, column v) is (c0 + j) V + v: the state advances by
+        // V golden-ratio increments per row
+        unsigned long long st = 0ull;
+        if (GUMBEL)
+            st = splitmix_state(p.seed, static_cast<unsigned long long>(c0) *
+                                                static_cast<unsigned>(p.V) +
+                                            static_cast<unsigned>(v));
         float my_tv[TOPK ? kMaxTopK : 1];
         int my_ti[TOPK ? kMaxTopK : 1];
 #pragma unroll
@@ -205,9 +217,8 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) ws += __shfl_xor_sync(0xFFFFFFFFu, ws, off);
             if (GUMBEL) {
-                const float g = gumbel_from_bits(uniform_bits24(
-                    p.seed, static_cast<unsigned long long>(row) * static_cast<unsigned>(p.V) +
-                                static_cast<unsigned>(v)));
+                const float g = gumbel_from_bits(bits24_from_state(st));
+                st += static_cast<unsigned long long>(static_cast<unsigned>(p.V)) * kGolden;
                 const float key = valid ? y + g : -INFINITY;
                 const uint32_t ok = float_to_ordered(key);
                 const uint32_t okm = __reduce_max_sync(0xFFFFFFFFu, ok);
@@ -401,18 +412,19 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
 #pragma unroll
         for (int j = 0; j < 32; ++j) rs += ex2_approx(fmaf(y[j], kLog2e, -mb));
         if (GUMBEL && rv) {
-            const unsigned long long nbase =
-                static_cast<unsigned long long>(row) * static_cast<unsigned>(p.V) +
-                static_cast<unsigned>(cb);
+            // consecutive columns are consecutive stream indices: the state advances by one
+            // golden-ratio increment per column
+            unsigned long long st = splitmix_state(
+                p.seed, static_cast<unsigned long long>(row) * static_cast<unsigned>(p.V) +
+                            static_cast<unsigned>(cb));
+            // columns past the shard end have y = -inf, so their key is -inf and never wins
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                if (j < nval) {
-                    const float key = y[j] + gumbel_from_bits(uniform_bits24(p.seed, nbase + j));
-                    if (key > gk) {
-                        gk = key;
-                        gi = cb + j;
-                        gz = __uint_as_float(raw[j]);
-                    }
+            for (int j = 0; j < 32; ++j, st += kGolden) {
+                const float key = y[j] + gumbel_from_bits(bits24_from_state(st));
+                if (key > gk) {
+                    gk = key;
+                    gi = cb + j;
+                    gz = __uint_as_float(raw[j]);
                 }
             }
         }
