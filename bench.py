@@ -45,6 +45,8 @@ WORKLOADS = {
                      desc="decode full-logit: H[64,4096] x W[151936,4096] bf16, k=2, FULL_LOGITS"),
     "prefill": dict(M=4096, d=6144, V=200064, k=4, surface="token_logprob", targets=True,
                     desc="prefill scoring: H[4096,6144] x W[200064,6144] bf16, k=4, lse + target log-prob"),
+    "decode64_token": dict(M=64, d=4096, V=151936, k=2, surface="token_logprob",
+                           desc="decode token-only at the full-logit shape: H[64,4096] x W[151936,4096] bf16, k=2"),
     "sampling": dict(M=256, d=5120, V=151936, k=4, surface="gumbel_token", T=0.7, seed=1234,
                      desc="seeded sampling: H[256,5120] x W[151936,5120] bf16, k=4, GUMBEL_TOKEN T=0.7"),
     "decode16_sample": dict(M=16, d=5120, V=151936, k=4, surface="gumbel_token", T=0.7,
@@ -81,14 +83,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # null once the source differs.
 KERNEL_TRAFFIC = {
     # decode16: dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
-    # (1,556,177,664 + 3,352,576 B; W + H are 1,555,988,480 B).
-    "decode16": {"bytes": 1559530240, "src_sha": "1d906b56533447fb"},
+    # (1,556,155,136 + 2,895,872 B; W + H are 1,555,988,480 B).
+    "decode16": {"bytes": 1559051008, "src_sha": "ba4bb169602a4e17"},
 }
 
 
 def kernel_src_hash() -> str:
     h = hashlib.sha256()
-    for f in ("lmhead.cu", "sb_ptx.cuh", "sb_internal.h"):
+    for f in ("lmhead.cu", "sb_ptx.cuh", "sb_pipe.cuh", "sb_gumbel.cuh", "sb_internal.h"):
         with open(os.path.join(ROOT, "gemm_epilogue_reduction_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
