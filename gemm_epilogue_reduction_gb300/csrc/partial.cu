@@ -7,15 +7,24 @@
 // output, and the partials must be summed (the completion obligation, Section 3.5) before
 // any consumer observes the value.  Here the lanes are on one GPU:
 //   Y[m][n] = sum over lanes l of P_l[m][n],  P_l = X[:, lane l] · W[:, lane l]^T.
-// Each lane's slice is cut into equal chunks of 64-column K blocks so the work fills the
-// GPU; `partial_kernel` writes one fp32 partial per (chunk, 128-feature tile) from a
-// tcgen05 accumulator, and `complete_kernel` sums the chunks in ascending order -- lane 0's
-// chunks first -- so the result bits never depend on scheduling.
 //
-// partial_kernel: persistent, 192 threads.  Warp 0 issues TMA loads of W (128 rows, the
-// UMMA A operand) and X (all M rows, the B operand) into one ring; warp 1 owns TMEM (two
-// accumulators) and issues tcgen05.mma; warps 2-5 read the accumulator (warp w reads TMEM
-// lanes 32*(w%4)..) and store the partial tile.  All waits are time-bounded (sb_pipe.cuh).
+// Work split.  The work is the sequence of (128-feature tile, 64-column K block) pairs, tile
+// by tile and K block by K block within a tile; CTA i of G takes a contiguous run of q or
+// q + 1 of them (q = work / G), so every CTA streams the same number of W bytes to within
+// one K block.  Each lane's slice of a tile (a "chunk") is covered by consecutive CTAs, and
+// a CTA's share of one chunk (a "piece") is accumulated in TMEM and stored as an fp32 slab
+// [M][128] at slot (chunk, CTA - first CTA of the chunk).
+//
+// Completion.  `complete_kernel`, launched as a programmatic dependent of `partial_kernel`
+// (it waits for that grid before reading), gives every thread four features of one row of
+// Y: it sums the tile's slabs in ascending K order -- lane 0's first -- and writes Y.  The
+// summation order is fixed, so the result bits never depend on scheduling.
+//
+// partial_kernel: persistent, 224 threads.  Warp 0 issues TMA loads of W (128 rows, the
+// UMMA A operand) into the W ring, warp 6 loads of X (all M rows, the B operand) into the X
+// ring; warp 1 owns TMEM (two accumulators) and issues tcgen05.mma; warps 2-5 read the
+// accumulator (warp w reads TMEM lanes 32*(w%4)..) and store the slab.  All waits are
+// time-bounded (sb_pipe.cuh).
 #include <cuda_bf16.h>
 
 #include <atomic>
@@ -29,22 +38,37 @@
 namespace sb {
 namespace {
 
-constexpr int kPThreads = 192;
-constexpr uint32_t kPStageA = kTileA * kBlockK * 2;  // 16 KB of W per stage
+constexpr int kPThreads = 224;
+constexpr int kPProducerX = 6;                       // warp loading X
+constexpr uint32_t kPStageW = kTileA * kBlockK * 2;  // 16 KB of W per stage
 constexpr int kPMaxStages = 16;
-constexpr int kMinUnits = 1300;                      // chunking target (many short units)
+constexpr int kPStagesX = 4;
+constexpr int kPMaxGrid = 1024;
 
 struct PartialParams {
-    int M, N, K, nb, kb_per_chunk, chunks, n_tiles, num_units, stages;
-    float *partials;  // [chunks][M][N]
+    int M, N, nb, kb_tile, lanes, lane_kb, n_tiles, grid, pieces, stages_w, stages_x;
+    uint32_t q, r;                   // CTA i owns q + 1 K blocks if i < r, else q
+    float *partials;                 // [n_tiles * lanes][pieces][M][128]
+    float *yf;                       // Y as fp32, or
+    uint16_t *yb;                    // Y as bf16 bits
     uint32_t *epoch_word;
     unsigned long long *status;
     uint32_t epoch;
     unsigned long long timeout_ns;
 };
 
-__host__ __device__ inline uint32_t p_smem_bytes(int nb, int stages) {
-    return stages * (kPStageA + nb * 128) + (2 * kPMaxStages + 8) * 8 + 16 + 1024;
+__host__ __device__ inline uint32_t p_smem_bytes(int nb, int stages_w, int stages_x) {
+    return stages_w * kPStageW + stages_x * nb * 128 + (4 * kPMaxStages + 8) * 8 + 16 + 1024;
+}
+
+// First work index of CTA i, and the CTA that owns work index x (all 32-bit: the work
+// count is checked against 2^31 on the host).
+__host__ __device__ inline uint32_t cta_begin(uint32_t q, uint32_t r, uint32_t i) {
+    return i * q + (i < r ? i : r);
+}
+__host__ __device__ inline uint32_t cta_of(uint32_t q, uint32_t r, uint32_t x) {
+    const uint32_t big = r * (q + 1);
+    return x < big ? x / (q + 1) : r + (x - big) / q;
 }
 
 __device__ __forceinline__ bool p_vote_any(bool pred) {  // over the 128 epilogue threads
@@ -66,25 +90,34 @@ __global__ void __launch_bounds__(kPThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    const uint32_t b_bytes = static_cast<uint32_t>(p.nb) * 128u;
-    uint8_t *sA = smem;
-    uint8_t *sB = smem + p.stages * kPStageA;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + p.stages * b_bytes);
-    uint64_t *full = bars;
-    uint64_t *empty = bars + kPMaxStages;
-    uint64_t *tfull = bars + 2 * kPMaxStages;
+    const uint32_t x_bytes = static_cast<uint32_t>(p.nb) * 128u;
+    uint8_t *sW = smem;
+    uint8_t *sX = smem + p.stages_w * kPStageW;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sX + p.stages_x * x_bytes);
+    uint64_t *fullW = bars;
+    uint64_t *emptyW = bars + kPMaxStages;
+    uint64_t *fullX = bars + 2 * kPMaxStages;
+    uint64_t *emptyX = bars + 3 * kPMaxStages;
+    uint64_t *tfull = bars + 4 * kPMaxStages;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kPMaxStages + 8);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 4 * kPMaxStages + 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const WaitCtx wc{p.status, p.epoch, p.timeout_ns, abort_flag};
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t x_begin = cta_begin(p.q, p.r, blockIdx.x);
+    const uint32_t x_end = x_begin + p.q + (blockIdx.x < p.r ? 1u : 0u);
+    const uint32_t first_cut = (x_begin / p.lane_kb + 1) * p.lane_kb;  // next lane boundary
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < p.stages; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+        for (int i = 0; i < p.stages_w; ++i) {
+            mbar_init(&fullW[i], 1);
+            mbar_init(&emptyW[i], 1);
+        }
+        for (int i = 0; i < p.stages_x; ++i) {
+            mbar_init(&fullX[i], 1);
+            mbar_init(&emptyX[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
@@ -105,87 +138,106 @@ __global__ void __launch_bounds__(kPThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // let the completion (a programmatic dependent launch) get scheduled early; it waits for
+    // this whole grid before it reads any slab
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    if (warp == 0) {
-        if (lane == 0) {  // TMA producer
-            const uint64_t pol_w = policy_evict_first();
-            const uint64_t pol_x = policy_evict_last();
+    if (warp == 0 || warp == kPProducerX) {
+        if (lane == 0) {  // TMA producers: the CTA's K blocks in order, one ring each
+            const bool is_w = warp == 0;
+            const int stages = is_w ? p.stages_w : p.stages_x;
+            const uint32_t bytes = is_w ? kPStageW : x_bytes;
+            uint8_t *ring = is_w ? sW : sX;
+            uint64_t *full = is_w ? fullW : fullX;
+            uint64_t *empty = is_w ? emptyW : emptyX;
+            const CUtensorMap *tm = is_w ? &tmW : &tmX;
+            const uint64_t pol = is_w ? policy_evict_first() : policy_evict_last();
             int stage = 0;
             uint32_t phase = 0, issued = 0;
-            bool ok = true;
-            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-                const int chunk = u / p.n_tiles, nt = u - chunk * p.n_tiles;
-                const int kb0 = chunk * p.kb_per_chunk;
-                for (int kb = kb0; kb < kb0 + p.kb_per_chunk; ++kb) {
-                    if (!bwait(&empty[stage], phase ^ 1u, wc)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&full[stage], kPStageA + b_bytes);
-                    tma_load_2d(sA + stage * kPStageA, &tmW, &full[stage], kb * kBlockK,
-                                nt * kTileA, pol_w);
-                    tma_load_2d(sB + stage * b_bytes, &tmX, &full[stage], kb * kBlockK, 0, pol_x);
-                    ++issued;
-                    if (++stage == p.stages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+            int tile = static_cast<int>(x_begin / p.kb_tile);
+            int kb = static_cast<int>(x_begin) - tile * p.kb_tile;
+            for (uint32_t x = x_begin; x < x_end; ++x) {
+                if (!bwait(&empty[stage], phase ^ 1u, wc)) break;
+                mbar_arrive_expect_tx(&full[stage], bytes);
+                tma_load_2d(ring + stage * bytes, tm, &full[stage], kb * kBlockK,
+                            is_w ? tile * kTileA : 0, pol);
+                ++issued;
+                if (++stage == stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                if (++kb == p.kb_tile) {
+                    kb = 0;
+                    ++tile;
                 }
             }
-            const uint32_t n = issued < static_cast<uint32_t>(p.stages) ? issued : p.stages;
+            const uint32_t n = issued < static_cast<uint32_t>(stages) ? issued : stages;
             for (uint32_t i = issued - n; i < issued; ++i)
-                bwait_drain(&full[i % p.stages], (i / p.stages) & 1u, wc);
+                bwait_drain(&full[i % stages], (i / stages) & 1u, wc);
         }
     } else if (warp == 1) {
-        if (lane == 0) {  // MMA issuer
+        if (lane == 0) {  // MMA issuer: one accumulation per piece
             const uint32_t idesc = idesc_bf16_f32(kTileA, p.nb);
-            int stage = 0, it = 0;
-            uint32_t phase = 0;
+            int sw = 0, sx = 0, j = 0;
+            uint32_t pw = 0, px = 0;
             bool ok = true, any = false;
-            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
-                const int b = it & 1;
-                if (!bwait(&tempty[b], ((it >> 1) & 1) ^ 1u, wc)) break;
+            uint32_t cut = first_cut;
+            for (uint32_t x = x_begin; ok && x < x_end; ++j, cut += p.lane_kb) {
+                const uint32_t e = cut < x_end ? cut : x_end;
+                const int b = j & 1;
+                if (!bwait(&tempty[b], ((j >> 1) & 1) ^ 1u, wc)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * p.nb);
-                for (int kb = 0; kb < p.kb_per_chunk; ++kb) {
-                    if (!bwait(&full[stage], phase, wc)) {
+                for (uint32_t xx = x; xx < e; ++xx) {
+                    if (!bwait(&fullW[sw], pw, wc) || !bwait(&fullX[sx], px, wc)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * kPStageA));
-                    const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * b_bytes));
+                    const uint64_t adesc = sw128_kmajor_desc(smem_u32(sW + sw * kPStageW));
+                    const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sX + sx * x_bytes));
 #pragma unroll
                     for (int ks = 0; ks < kBlockK / 16; ++ks)
                         umma_bf16(d_tmem, adesc + 2u * ks, bdesc + 2u * ks, idesc,
-                                  (kb | ks) != 0 ? 1u : 0u);
-                    umma_commit(&empty[stage]);
+                                  (xx != x || ks != 0) ? 1u : 0u);
+                    umma_commit(&emptyW[sw]);
+                    umma_commit(&emptyX[sx]);
                     any = true;
-                    if (++stage == p.stages) {
-                        stage = 0;
-                        phase ^= 1u;
+                    if (++sw == p.stages_w) {
+                        sw = 0;
+                        pw ^= 1u;
+                    }
+                    if (++sx == p.stages_x) {
+                        sx = 0;
+                        px ^= 1u;
                     }
                 }
                 if (ok) umma_commit(&tfull[b]);
+                x = e;
             }
             if (any) {
                 umma_commit(drain);
                 bwait_drain(drain, 0, wc);
             }
         }
-    } else {  // epilogue: thread = output feature n, TMEM columns = rows m
+    } else if (warp >= 2 && warp <= 5) {
+        // epilogue: thread = output feature of the tile, TMEM columns = rows m
         const int q = warp & 3;
-        int it = 0;
-        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++it) {
-            const int b = it & 1;
-            const bool ok = bwait(&tfull[b], (it >> 1) & 1, wc);
+        const int nl = 32 * q + lane;
+        int j = 0;
+        uint32_t cut = first_cut;
+        for (uint32_t x = x_begin; x < x_end; ++j, cut += p.lane_kb) {
+            const uint32_t e = cut < x_end ? cut : x_end;
+            const uint32_t chunk = x / p.lane_kb;
+            const uint32_t piece = blockIdx.x - cta_of(p.q, p.r, chunk * p.lane_kb);
+            const int b = j & 1;
+            const bool ok = bwait(&tfull[b], (j >> 1) & 1, wc);
             if (p_vote_any(!ok)) break;
             tc_fence_after();
-            const int chunk = u / p.n_tiles, nt = u - chunk * p.n_tiles;
-            const int n = nt * kTileA + 32 * q + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                                    static_cast<uint32_t>(b * p.nb);
-            float *dst = p.partials + static_cast<size_t>(chunk) * p.M * p.N + n;
+            float *dst = p.partials +
+                         (static_cast<size_t>(chunk) * p.pieces + piece) * p.M * kTileA + nl;
             for (int c0 = 0; c0 < p.nb; c0 += 32) {
                 uint32_t raw[32];
                 const int cw = min(32, p.nb - c0);
@@ -198,13 +250,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&tempty[b]);
                 }
-                if (n < p.N) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (j < cw && c0 + j < p.M)
-                            dst[static_cast<size_t>(c0 + j) * p.N] = __uint_as_float(raw[j]);
-                }
+                for (int jj = 0; jj < 32; ++jj)
+                    if (jj < cw && c0 + jj < p.M)
+                        dst[static_cast<size_t>(c0 + jj) * kTileA] = __uint_as_float(raw[jj]);
             }
+            x = e;
         }
     }
     tc_fence_before();
@@ -216,44 +267,113 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
 }
 
-// Y[i] = sum over chunks c (ascending) of partials[c][i]; fp32 or bf16 (round to nearest).
-__global__ void complete_kernel(const float *__restrict__ partials, int chunks, size_t mn,
-                                float *yf, uint16_t *yb) {
+// Y[m][n] = the left fold over the tile's slabs, in ascending K order, of slab[m][n % 128];
+// one thread per four features of one row.  Slabs are read in batches of kBatch, all loads
+// of a batch issued before its adds.
+__global__ void __launch_bounds__(256)
+    complete_kernel(const PartialParams p) {
+    constexpr int kBatch = 8;
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < mn;
-         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-        float acc = 0.f;
-        for (int c = 0; c < chunks; ++c) acc += __ldg(partials + c * mn + i);
-        if (yb)
-            yb[i] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
-        else
-            yf[i] = acc;
+    const size_t items = static_cast<size_t>(p.n_tiles) * p.M * (kTileA / 4);
+    for (size_t it = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; it < items;
+         it += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const int f4 = static_cast<int>(it % (kTileA / 4));
+        const int m = static_cast<int>((it / (kTileA / 4)) % p.M);
+        const int tile = static_cast<int>(it / (static_cast<size_t>(kTileA / 4) * p.M));
+        const int n0 = tile * kTileA + 4 * f4;
+        if (n0 >= p.N) continue;
+        const float *base = p.partials + static_cast<size_t>(m) * kTileA + 4 * f4;
+        const size_t slab = static_cast<size_t>(p.M) * kTileA;
+        // walk (lane l, CTA i) over the tile's chunks: slot = chunk * pieces + (i - a)
+        int l = 0;
+        uint32_t c = static_cast<uint32_t>(tile * p.lanes);
+        uint32_t a = cta_of(p.q, p.r, c * p.lane_kb);
+        uint32_t b = cta_of(p.q, p.r, c * p.lane_kb + p.lane_kb - 1);
+        uint32_t i = a;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        while (l < p.lanes) {
+            float4 v[kBatch];
+            bool ok[kBatch];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                ok[k] = l < p.lanes;
+                if (ok[k]) {
+                    v[k] = __ldg(reinterpret_cast<const float4 *>(
+                        base + (static_cast<size_t>(c) * p.pieces + (i - a)) * slab));
+                    if (++i > b) {
+                        if (++l < p.lanes) {
+                            ++c;
+                            a = cta_of(p.q, p.r, c * p.lane_kb);
+                            b = cta_of(p.q, p.r, c * p.lane_kb + p.lane_kb - 1);
+                            i = a;
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                if (ok[k]) {
+                    acc.x += v[k].x;
+                    acc.y += v[k].y;
+                    acc.z += v[k].z;
+                    acc.w += v[k].w;
+                }
+            }
+        }
+        const float r4[4] = {acc.x, acc.y, acc.z, acc.w};
+        const size_t o = static_cast<size_t>(m) * p.N + n0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (n0 + u >= p.N) break;
+            if (p.yb)
+                p.yb[o + u] = __bfloat16_as_ushort(__float2bfloat16_rn(r4[u]));
+            else
+                p.yf[o + u] = r4[u];
+        }
     }
 }
 
-// Chunks per lane: the smallest divisor of the lane's K blocks giving at least kMinUnits
-// work units, but no more than keep the fp32 partials' round trip (write + read,
-// 8*lanes*chunks*M*N bytes) within about an eighth of W's bytes (2*N*K).  Chosen from the
-// shape alone, so the workspace size does not depend on the device.  (Measured on the
-// 5120 x 17408 down projection: 8 chunks per lane best at 64 tokens, 17 at 8 tokens.)
-int chunks_per_lane(int64_t M, int64_t N, int64_t K, int32_t lanes) {
-    const int64_t kb_lane = K / kBlockK / lanes;
-    const int64_t n_tiles = (N + kTileA - 1) / kTileA;
-    const int64_t cap = K / (16 * lanes * M);
-    int64_t best = 1;
-    for (int64_t c = 1; c <= kb_lane; ++c) {
-        if (kb_lane % c) continue;
-        if (c > cap && c > 1) break;
-        best = c;
-        if (n_tiles * lanes * c >= kMinUnits) break;
-    }
-    return static_cast<int>(best);
-}
+struct PartialPlan {
+    int grid, pieces, n_tiles, kb_tile, lane_kb;
+    uint32_t q, r;
+    size_t slab_off, bytes;
+};
 
 bool partial_shape_ok(int64_t M, int64_t N, int64_t K, int32_t lanes) {
     return M >= 1 && M <= kMaxVocabModeRows * 2 && N >= 1 && N < (int64_t(1) << 31) &&
            lanes >= 1 && K >= kBlockK && K < (int64_t(1) << 31) &&
            K % (static_cast<int64_t>(lanes) * kBlockK) == 0;
+}
+
+// The split for the current device: one CTA per SM (at most one per K block), the most
+// pieces any chunk has, and the workspace layout (header, then the slabs).
+int32_t make_plan(int64_t M, int64_t N, int64_t K, int32_t lanes, PartialPlan *pl) {
+    if (!partial_shape_ok(M, N, K, lanes)) return SB_ERR_INVALID_ARG;
+    int sms = 0, cc = 0;
+    if (int32_t e = device_sms_cc(&sms, &cc)) return e;
+    const int64_t n_tiles = (N + kTileA - 1) / kTileA;
+    const int64_t work = n_tiles * (K / kBlockK);
+    if (work >= (int64_t(1) << 31)) return SB_ERR_UNSUPPORTED;
+    pl->n_tiles = static_cast<int>(n_tiles);
+    pl->kb_tile = static_cast<int>(K / kBlockK);
+    pl->lane_kb = pl->kb_tile / lanes;
+    int64_t g = sms < kPMaxGrid ? sms : kPMaxGrid;
+    if (g > work) g = work;
+    pl->grid = static_cast<int>(g);
+    pl->q = static_cast<uint32_t>(work / g);
+    pl->r = static_cast<uint32_t>(work % g);
+    const uint32_t lk = static_cast<uint32_t>(pl->lane_kb);
+    uint32_t pieces = 1;
+    const int64_t chunks = n_tiles * lanes;
+    for (int64_t c = 0; c < chunks; ++c) {
+        const uint32_t c0 = static_cast<uint32_t>(c) * lk;
+        const uint32_t n = cta_of(pl->q, pl->r, c0 + lk - 1) - cta_of(pl->q, pl->r, c0) + 1;
+        pieces = n > pieces ? n : pieces;
+    }
+    pl->pieces = static_cast<int>(pieces);
+    pl->slab_off = 256;
+    pl->bytes = pl->slab_off + static_cast<size_t>(chunks) * pieces * M * kTileA * 4;
+    return SB_OK;
 }
 
 }  // namespace
@@ -262,10 +382,8 @@ bool partial_shape_ok(int64_t M, int64_t N, int64_t K, int32_t lanes) {
 extern "C" {
 
 size_t sb_partial_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t lanes) {
-    using namespace sb;
-    if (!partial_shape_ok(M, N, K, lanes)) return 0;
-    const int64_t chunks = static_cast<int64_t>(lanes) * chunks_per_lane(M, N, K, lanes);
-    return 256 + static_cast<size_t>(chunks) * M * N * 4;
+    sb::PartialPlan pl;
+    return sb::make_plan(M, N, K, lanes, &pl) == SB_OK ? pl.bytes : 0;
 }
 
 int32_t sb_partial_completion(const void *X, const void *W, int64_t M, int64_t N, int64_t K,
@@ -278,34 +396,39 @@ int32_t sb_partial_completion(const void *X, const void *W, int64_t M, int64_t N
           reinterpret_cast<uintptr_t>(workspace) % 256 == 0 &&
           reinterpret_cast<uintptr_t>(Y) % (y_bf16 ? 2 : 4) == 0))
         return SB_ERR_ALIGNMENT;
-    const size_t need = sb_partial_workspace_bytes(M, N, K, lanes);
-    if (workspace_bytes < need) return SB_ERR_WORKSPACE_TOO_SMALL;
-    int sms = 0, cc = 0;
-    if (int32_t e = device_sms_cc(&sms, &cc)) return e;
+    PartialPlan pl;
+    if (int32_t e = make_plan(M, N, K, lanes, &pl)) return e;
+    if (workspace_bytes < pl.bytes) return SB_ERR_WORKSPACE_TOO_SMALL;
 
     PartialParams p{};
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
-    p.K = static_cast<int>(K);
     p.nb = static_cast<int>((M + 15) / 16 * 16);
-    const int cpl = chunks_per_lane(M, N, K, lanes);
-    p.kb_per_chunk = static_cast<int>(K / kBlockK / lanes / cpl);
-    p.chunks = lanes * cpl;
-    p.n_tiles = static_cast<int>((N + kTileA - 1) / kTileA);
-    p.num_units = p.chunks * p.n_tiles;
-    p.stages = kPMaxStages;
-    while (p.stages > 2 && p_smem_bytes(p.nb, p.stages) > kSmemLimit) --p.stages;
+    p.kb_tile = pl.kb_tile;
+    p.lanes = lanes;
+    p.lane_kb = pl.lane_kb;
+    p.n_tiles = pl.n_tiles;
+    p.grid = pl.grid;
+    p.pieces = pl.pieces;
+    p.q = pl.q;
+    p.r = pl.r;
+    p.stages_x = kPStagesX;
+    p.stages_w = kPMaxStages;
+    while (p.stages_w > 2 && p_smem_bytes(p.nb, p.stages_w, p.stages_x) > kSmemLimit)
+        --p.stages_w;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     p.epoch_word = reinterpret_cast<uint32_t *>(ws);
     p.status = reinterpret_cast<unsigned long long *>(ws + 8);
-    p.partials = reinterpret_cast<float *>(ws + 256);
+    p.partials = reinterpret_cast<float *>(ws + pl.slab_off);
+    p.yf = y_bf16 ? nullptr : static_cast<float *>(Y);
+    p.yb = y_bf16 ? static_cast<uint16_t *>(Y) : nullptr;
     p.epoch = next_epoch();
     p.timeout_ns = wait_limit_ns();
 
     CUtensorMap tmW, tmX;
     if (!encode_bf16_map(&tmW, W, N, K, kTileA) || !encode_bf16_map(&tmX, X, M, K, p.nb))
         return SB_ERR_CUDA;
-    const size_t smem = p_smem_bytes(p.nb, p.stages);
+    const size_t smem = p_smem_bytes(p.nb, p.stages_w, p.stages_x);
     static std::atomic<uint64_t> opted_in{0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SB_ERR_CUDA;
@@ -318,27 +441,25 @@ int32_t sb_partial_completion(const void *X, const void *W, int64_t M, int64_t N
     }
     uint32_t cols = 32;
     while (cols < static_cast<uint32_t>(2 * p.nb)) cols <<= 1;
-    const int grid = p.num_units < sms ? p.num_units : sms;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    partial_kernel<<<grid, kPThreads, smem, st>>>(tmW, tmX, p, cols);
+    partial_kernel<<<p.grid, kPThreads, smem, st>>>(tmW, tmX, p, cols);
     if (cudaGetLastError() != cudaSuccess) return SB_ERR_CUDA;
 
-    const size_t mn = static_cast<size_t>(M) * N;
+    int sms = 0, cc = 0;
+    if (int32_t e = device_sms_cc(&sms, &cc)) return e;
+    const size_t items = static_cast<size_t>(p.n_tiles) * p.M * (kTileA / 4);
+    const size_t blocks = (items + 255) / 256;
+    const size_t cap = static_cast<size_t>(sms) * 8;
     cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks < cap ? blocks : cap));
     cfg.blockDim = dim3(256);
-    const size_t blocks = (mn + 255) / 256;
-    cfg.gridDim = dim3(static_cast<unsigned>(blocks < 4096 ? blocks : 4096));
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    float *yf = y_bf16 ? nullptr : static_cast<float *>(Y);
-    uint16_t *yb = y_bf16 ? static_cast<uint16_t *>(Y) : nullptr;
-    if (cudaLaunchKernelEx(&cfg, complete_kernel, static_cast<const float *>(p.partials),
-                           p.chunks, mn, yf, yb) != cudaSuccess)
-        return SB_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, complete_kernel, p) != cudaSuccess) return SB_ERR_CUDA;
     return SB_OK;
 }
 

@@ -263,11 +263,15 @@ int32_t sb_merge_shard_payload(const void *payload, int64_t M, int32_t k, int32_
  *   lanes      >= 1.
  *   Y          device [M, N] row-major: fp32 when y_bf16 == 0, else bf16 (round to nearest).
  *   workspace  device, 256-byte aligned, >= sb_partial_workspace_bytes(M, N, K, lanes):
- *              header (read by sb_last_device_status) + fp32 partials; no initialisation.
- * Each lane's slice is cut into equal chunks so the work fills the GPU; the partials are
- * accumulated in fp32 on the tensor cores and summed in ascending chunk order (lane 0's
- * chunks first), so the result bits do not depend on scheduling.  Two kernels are enqueued
- * on stream; returns SB_OK or an error with nothing enqueued.
+ *              header (read by sb_last_device_status) and fp32 partials; no
+ *              initialisation.  One call at a time per workspace.
+ * The (128-feature tile, 64-column K block) work is split evenly over the SMs; each SM cuts
+ * its share at lane boundaries and accumulates every piece in fp32 on the tensor cores.  A
+ * second kernel (a programmatic dependent of the first) sums each tile's pieces in
+ * ascending K order (lane 0's first), so the result bits do not depend on scheduling.  Two
+ * kernels are enqueued on stream; returns SB_OK or an error with nothing enqueued.
+ * sb_partial_workspace_bytes depends on the shape and on the SM count of the current
+ * device; it returns 0 for an invalid shape or when no CUDA device is usable.
  */
 size_t sb_partial_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t lanes);
 int32_t sb_partial_completion(const void *X, const void *W, int64_t M, int64_t N, int64_t K,

@@ -30,6 +30,12 @@ def _inputs(M, N, K, seed, device="cpu"):
 @pytest.mark.parametrize("M,N,K,lanes", [
     (1, 384, 1024, 2), (8, 1000, 2048, 2), (17, 300, 512, 4), (64, 640, 1280, 5),
     (200, 130, 640, 1), (256, 257, 768, 3),
+    # several segments per CTA, and tiles summed in two row groups
+    (32, 2048, 8192, 16),
+    # one-block lanes: a tile of 512 slabs, summed in two batches through a running sum
+    (4, 128, 32768, 512),
+    # a single feature tile split over every CTA (152 slabs per tile on a 152-SM part)
+    (64, 128, 17408, 2),
 ])
 @pytest.mark.parametrize("bf16_out", [False, True])
 def test_partial_completion_parity(M, N, K, lanes, bf16_out):
@@ -43,11 +49,18 @@ def test_partial_completion_parity(M, N, K, lanes, bf16_out):
 
 
 def test_partial_completion_is_deterministic():
+    """Same bits from a fresh workspace and from a reused one (whose per-tile arrival
+    counters still hold the previous call's counts)."""
     X, W = _inputs(64, 512, 2048, seed=3)
-    a, _ = sb.partial_completion(X, W, 2, out_bf16=False)
+    a, ws = sb.partial_completion(X, W, 2, out_bf16=False)
     b, _ = sb.partial_completion(X, W, 2, out_bf16=False)
+    c, _ = sb.partial_completion(X, W, 2, out_bf16=False, workspace=ws)
+    X2, W2 = _inputs(64, 5120, 17408, seed=4)
+    d, ws2 = sb.partial_completion(X2, W2, 2, out_bf16=False)
+    e, _ = sb.partial_completion(X2, W2, 2, out_bf16=False, workspace=ws2)
     torch.cuda.synchronize()
-    assert torch.equal(a, b)
+    assert torch.equal(a, b) and torch.equal(a, c)
+    assert torch.equal(d, e)
 
 
 def _table3():
