@@ -71,6 +71,8 @@ WORKLOADS = {
                           desc="profiling case: H[1024,2048] x W[65536,2048] bf16, k=4"),
     "sampling_token_small": dict(M=256, d=5120, V=65536, k=4, surface="token_logprob",
                                  desc="profiling case: H[256,5120] x W[65536,5120] bf16, k=4"),
+    "decode16_topk_small": dict(M=16, d=1024, V=151936, k=4, surface="topk_logprob", topk=8,
+                                desc="profiling case: H[16,1024] x W[151936,1024] bf16, k=4, top-8"),
     "sampling_small": dict(M=256, d=1024, V=151936, k=4, surface="gumbel_token", T=0.7,
                            seed=1234,
                            desc="profiling case: H[256,1024] x W[151936,1024] bf16, k=4, GUMBEL"),

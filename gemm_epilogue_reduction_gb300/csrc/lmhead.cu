@@ -58,7 +58,7 @@ struct SmemLayout {
 // Shared memory: ring A (stages_a x 16 KB), ring B (stages_b x nb*128 B), mbarriers,
 // TMEM address + abort flag, vocab-mode target ids and cross-quadrant scratch.
 __host__ __device__ inline SmemLayout make_layout(int nb, int stages_a, int stages_b, bool vocab,
-                                                  int flags) {
+                                                  int flags, int topk) {
     SmemLayout L;
     uint32_t off = 0;
     L.a_off = off;
@@ -73,7 +73,8 @@ __host__ __device__ inline SmemLayout make_layout(int nb, int stages_a, int stag
     off += vocab ? kMaxVocabModeRows * 4 : 0;
     L.scratch_off = off;
     off += vocab ? 4 * nb * ((flags & kFlagGumbel) ? 24 : 12) : 0;
-    off += (vocab && (flags & kFlagTopk)) ? 4 * nb * kMaxTopK * 8 : 0;
+    // top-K: the quadrants' lists, values then columns
+    off += (vocab && (flags & kFlagTopk)) ? 4 * nb * topk * 8 : 0;
     L.total = off + 1024;  // slack to align the base to 1024 bytes
     return L;
 }
@@ -159,8 +160,8 @@ __device__ __forceinline__ uint16_t bf16_bits_rn(float z) {
 
 // ------------------------------------------------------------------ epilogue, vocab mode
 // Thread (warp quadrant q, lane) holds vocabulary column v = v0 + 32q + lane for every row
-// (TMEM columns).  The two warps of a quadrant take alternate 32-row chunks (half h takes
-// chunks h, h+2, ...).  Per row: warp max / lowest argmax / sum of exp with warp reductions,
+// (TMEM columns).  The two warps of a quadrant take alternate 8-row chunks (half h takes
+// chunks h, h+2, ...), so at M <= 16 each walks at most 8 rows.  Per row: warp max / lowest argmax / sum of exp with warp reductions,
 // then the four quadrants' partial records merge in quadrant order through shared memory.
 template <int EPI>
 __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCoord &c,
@@ -181,17 +182,15 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
     float *sc_gk = scratch + 12 * nb;
     int *sc_gi = reinterpret_cast<int *>(scratch + 16 * nb);
     float *sc_gz = scratch + 20 * nb;
-    // top-K scratch: [quadrant][row][kMaxTopK] values, then the same for columns
+    // top-K scratch: [quadrant][row][K] values, then the same for columns
     float *sc_tv = scratch + 12 * nb;
-    int *sc_ti = reinterpret_cast<int *>(sc_tv + 4 * nb * kMaxTopK);
+    int *sc_ti = reinterpret_cast<int *>(sc_tv + 4 * nb * K);
 
-    for (int c0 = 32 * h; c0 < nb; c0 += 64) {
-        uint32_t raw[32];
-        const int cw = min(32, nb - c0);
-        if (cw == 32)
-            tmem_ld32x32b_x32(taddr + c0, raw);
-        else
-            tmem_ld32x32b_x16(taddr + c0, raw);
+    // nb is a multiple of 16, so every chunk is 8 whole accumulator columns
+    for (int c0 = 8 * h; c0 < nb; c0 += 16) {
+        uint32_t raw[8];
+        constexpr int cw = 8;
+        tmem_ld32x32b_x8(taddr + c0, raw);
         float my_m = -INFINITY, my_s = 0.f, my_gk = -INFINITY, my_gz = 0.f;
         int my_i = INT_MAX, my_gi = INT_MAX;
         // stream index of (row c0 + j, column v) is (c0 + j) V + v: the state advances by
@@ -204,9 +203,9 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
         float my_tv[TOPK ? kMaxTopK : 1];
         int my_ti[TOPK ? kMaxTopK : 1];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < cw; ++j) {
             const int row = c0 + j;
-            if (j >= cw || row >= p.M) break;
+            if (row >= p.M) break;
             const float z = __uint_as_float(raw[j]);
             const float y = valid ? (GUMBEL ? z * p.inv_t : z) : -INFINITY;
             const uint32_t oy = float_to_ordered(y);
@@ -270,8 +269,8 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
 #pragma unroll
                 for (int r = 0; r < kMaxTopK; ++r) {
                     if (r >= K) break;
-                    sc_tv[o * kMaxTopK + r] = my_tv[r];
-                    sc_ti[o * kMaxTopK + r] = my_ti[r];
+                    sc_tv[o * K + r] = my_tv[r];
+                    sc_ti[o * K + r] = my_ti[r];
                 }
             }
         }
@@ -327,7 +326,7 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
                 for (int w = 0; w < 4; ++w) {
                     const int pw = w == 0 ? p0 : (w == 1 ? p1 : (w == 2 ? p2 : p3));
                     if (pw >= K) continue;
-                    const int o = (w * nb + row) * kMaxTopK + pw;
+                    const int o = (w * nb + row) * K + pw;
                     const float vw = sc_tv[o];
                     const int iw = sc_ti[o];
                     if (vw > bv || (vw == bv && iw < bi)) {
@@ -559,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    const SmemLayout L = make_layout(p.nb, p.stages_a, p.stages_b, VOCAB, p.flags);
+    const SmemLayout L = make_layout(p.nb, p.stages_a, p.stages_b, VOCAB, p.flags, p.topk);
     uint8_t *sA = smem + L.a_off;
     uint8_t *sB = smem + L.b_off;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
@@ -794,8 +793,9 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmP
 
 }  // namespace
 
-size_t lmhead_smem_bytes(int nb, int stages_a, int stages_b, bool vocab_mode, int flags) {
-    return make_layout(nb, stages_a, stages_b, vocab_mode, flags).total;
+size_t lmhead_smem_bytes(int nb, int stages_a, int stages_b, bool vocab_mode, int flags,
+                         int topk) {
+    return make_layout(nb, stages_a, stages_b, vocab_mode, flags, topk).total;
 }
 
 cudaError_t launch_lmhead(bool vocab_mode, const CUtensorMap &tmA, const CUtensorMap &tmB,

@@ -202,18 +202,18 @@ int32_t check_outputs(const sb_outputs *out, int32_t surface, bool need_ws) {
 
 // Ring depths: the ring of the operand re-read from L2 (H) gets a fixed depth, the ring of
 // the operand streamed from HBM (W) every remaining stage that fits in shared memory.
-bool pick_stages(int nb, bool vm, int m_tiles, int flags, int *sa, int *sb) {
+bool pick_stages(int nb, bool vm, int m_tiles, int flags, int topk, int *sa, int *sb) {
     (void)m_tiles;
     if (vm) {  // A = W (streamed), B = H
         *sb = SB_VOCAB_STAGES_B;
         for (*sa = kMaxStages; *sa > 1; --*sa)
-            if (lmhead_smem_bytes(nb, *sa, *sb, vm, flags) <= kSmemLimit) break;
+            if (lmhead_smem_bytes(nb, *sa, *sb, vm, flags, topk) <= kSmemLimit) break;
     } else {   // A = H, B = W tile (streamed or shared by the cluster)
         *sa = SB_ROWS_STAGES_A;
         for (*sb = kMaxStages; *sb > 1; --*sb)
-            if (lmhead_smem_bytes(nb, *sa, *sb, vm, flags) <= kSmemLimit) break;
+            if (lmhead_smem_bytes(nb, *sa, *sb, vm, flags, topk) <= kSmemLimit) break;
     }
-    return lmhead_smem_bytes(nb, *sa, *sb, vm, flags) <= kSmemLimit && *sa >= 2 && *sb >= 2;
+    return lmhead_smem_bytes(nb, *sa, *sb, vm, flags, topk) <= kSmemLimit && *sa >= 2 && *sb >= 2;
 }
 
 CombineParams combine_params(const sb_outputs *out, const Workspace &w, int64_t M, int32_t k,
@@ -315,7 +315,8 @@ int32_t enqueue(const void *H, const void *W, int64_t M, int64_t d, int64_t V, i
     if (tiles >= (int64_t(1) << 31)) return SB_ERR_INVALID_ARG;
     p.num_tiles = static_cast<int>(tiles);
     p.kblocks = static_cast<int>((d + kBlockK - 1) / kBlockK);
-    if (!pick_stages(p.nb, vm, p.m_tiles, flags, &p.stages_a, &p.stages_b)) return SB_ERR_UNSUPPORTED;
+    if (!pick_stages(p.nb, vm, p.m_tiles, flags, K, &p.stages_a, &p.stages_b))
+        return SB_ERR_UNSUPPORTED;
     p.flags = flags;
     p.topk = K;
     p.inv_t = inv_t;
@@ -333,7 +334,7 @@ int32_t enqueue(const void *H, const void *W, int64_t M, int64_t d, int64_t V, i
                        : (make_map(&tmA, H, M, d, kTileA) &&
                           make_map(&tmB, W, V, d, kRowsTileN / p.cluster));
     if (!ok) return SB_ERR_CUDA;
-    const size_t smem = lmhead_smem_bytes(p.nb, p.stages_a, p.stages_b, vm, flags);
+    const size_t smem = lmhead_smem_bytes(p.nb, p.stages_a, p.stages_b, vm, flags, K);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (launch_lmhead(vm, tmA, tmB, p, smem, dev.sms, st) != cudaSuccess) return SB_ERR_CUDA;
     if (!with_combine) return SB_OK;

@@ -96,7 +96,8 @@ cudaError_t launch_pack(const Workspace &ws, int M, int k, int T, bool gumbel,
 cudaError_t launch_merge_payload(const CombineParams &c, const void *payload,
                                  cudaStream_t stream);
 
-size_t lmhead_smem_bytes(int nb, int stages_a, int stages_b, bool vocab_mode, int flags);
+size_t lmhead_smem_bytes(int nb, int stages_a, int stages_b, bool vocab_mode, int flags,
+                         int topk);
 
 // Host helpers shared by the entry points (sb_api.cu).
 bool encode_bf16_map(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols,

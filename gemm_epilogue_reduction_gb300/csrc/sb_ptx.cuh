@@ -166,6 +166,15 @@ __device__ __forceinline__ void cluster_sync() {
 // TMEM -> registers, 32 lanes x 32 bits: thread t of the warp reads lane (base lane + t),
 // columns [col, col + N).  The wait is inside the same statement so the outputs are never
 // used before the load has landed.
+__device__ __forceinline__ void tmem_ld32x32b_x8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+}
 __device__ __forceinline__ void tmem_ld32x32b_x16(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
