@@ -30,6 +30,10 @@
  *     and read with sb_last_device_status() after the caller synchronises.
  *   - There is no CPU fallback: a device that is not sm_103 returns SB_ERR_UNSUPPORTED.
  *   - Calls that share a workspace must not overlap on the GPU (they would race on it).
+ *   - The calls enqueue kernels only (no host synchronisation), so they can be captured in
+ *     a CUDA graph; arguments are checked and tensor maps encoded at capture time.  Every
+ *     replay then carries the captured call's launch epoch, so after replays
+ *     sb_last_device_status reports the worst device status since the capture.
  */
 #ifndef SB_H
 #define SB_H
