@@ -161,8 +161,9 @@ __device__ __forceinline__ uint16_t bf16_bits_rn(float z) {
 // ------------------------------------------------------------------ epilogue, vocab mode
 // Thread (warp quadrant q, lane) holds vocabulary column v = v0 + 32q + lane for every row
 // (TMEM columns).  The two warps of a quadrant take alternate 8-row chunks (half h takes
-// chunks h, h+2, ...), so at M <= 16 each walks at most 8 rows.  Per row: warp max / lowest argmax / sum of exp with warp reductions,
-// then the four quadrants' partial records merge in quadrant order through shared memory.
+// chunks h, h+2, ...), so at M <= 16 each walks at most 8 rows.  Per row: warp max, lowest
+// argmax and sum of exp with warp reductions; then the four quadrants' partial records
+// merge in quadrant order through shared memory.
 template <int EPI>
 __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCoord &c,
                                                uint32_t taddr, uint64_t *tempty_b, int q,
@@ -239,7 +240,8 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
                     if (r >= K) break;
                     const uint32_t oc = alive ? oy : float_to_ordered(-INFINITY);
                     const uint32_t ocm = __reduce_max_sync(0xFFFFFFFFu, oc);
-                    const int ci = __reduce_min_sync(0xFFFFFFFFu, (alive && oc == ocm) ? v : INT_MAX);
+                    const int ci =
+                        __reduce_min_sync(0xFFFFFFFFu, (alive && oc == ocm) ? v : INT_MAX);
                     if (v == ci) alive = false;
                     if (lane == j) {
                         my_tv[r] = ordered_to_float(ocm);

@@ -17,11 +17,11 @@ constexpr int kRecordCols = 128;     // vocabulary columns covered by one projec
 #endif
 constexpr int kMaxVocabModeRows = SB_MAX_VOCAB_MODE_ROWS;  // largest M with W as the A operand
 constexpr int kMaxStages = 16;
-constexpr int kMaxShards = 1024;
+constexpr int kMaxShards = 1024;  // largest k (the combine keeps k shard records in smem)
 #ifndef SB_ROWS_CLUSTER
 #define SB_ROWS_CLUSTER 2
 #endif
-constexpr int kRowsCluster = SB_ROWS_CLUSTER;  // rows mode: CTAs (consecutive M tiles) per W tile     // largest k (the combine keeps k shard records in smem)
+constexpr int kRowsCluster = SB_ROWS_CLUSTER;  // rows mode: CTAs (consecutive M tiles) per W tile
 constexpr int kEpiWarps = 8;         // two epilogue warps per TMEM lane quadrant
 constexpr int kFirstEpiWarp = 3;     // warps 0 and 2 load, warp 1 issues MMAs + owns TMEM
 constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
