@@ -64,7 +64,8 @@ __host__ __device__ inline SmemLayout make_layout(int nb, int stages_a, int stag
     L.a_off = off;
     off += stages_a * kStageBytesA;
     L.b_off = off;
-    off += stages_b * nb * 128;
+    // rows mode with CTA pairs: each CTA stages only its half of the W tile
+    off += stages_b * ((!vocab && kRowsPair) ? nb / 2 : nb) * 128;
     L.bar_off = off;
     off += (4 * kMaxStages + 8) * 8;
     L.misc_off = off;
@@ -109,9 +110,14 @@ __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, volatile i
                                       const GemmParams &p) {
     return bwait(bar, parity, wait_ctx(p, abort_flag));
 }
-__device__ __forceinline__ void bwait_drain(uint64_t *bar, uint32_t parity,
+__device__ __forceinline__ bool bwait_drain(uint64_t *bar, uint32_t parity,
                                             volatile int *abort_flag, const GemmParams &p) {
-    bwait_drain(bar, parity, wait_ctx(p, abort_flag));
+    return bwait_drain(bar, parity, wait_ctx(p, abort_flag));
+}
+// For barriers armed from the other CTA of a pair (cluster-scope acquire).
+__device__ __forceinline__ bool bwait_cl(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                         const GemmParams &p) {
+    return bwait_cluster(bar, parity, wait_ctx(p, abort_flag));
 }
 
 __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
@@ -354,10 +360,12 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
 // [v0 + 128h, v0 + 128h + 128) of the 256-column tile, i.e. record tile 2t + h.  It walks
 // them in chunks of 32: chunk max and first argmax, online rescale of the running sum, then
 // the sum of exp against the running max.
+// tempty_remote: the cluster address of the pair leader's accumulator-empty barrier when this
+// CTA is the peer of a CTA pair (0: arrive on tempty_b in this CTA).
 template <int EPI>
 __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoord &c,
                                               uint32_t taddr, uint64_t *tempty_b, int q, int h,
-                                              int lane) {
+                                              int lane, uint32_t tempty_remote) {
     constexpr bool GUMBEL = EPI == kEpiGumbel;
     constexpr bool FULL = EPI == kEpiFull;
     constexpr bool TOPK = EPI == kEpiTopk;
@@ -387,7 +395,12 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
         if (ch == kChunks - 1) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_b);
+            if (lane == 0) {
+                if (tempty_remote)
+                    mbar_arrive_remote(tempty_remote);
+                else
+                    mbar_arrive(tempty_b);
+            }
         }
         const int cb = cbase0 + ch * 32;
         const int nval = min(32, c.v_end - cb);
@@ -514,7 +527,13 @@ __device__ __forceinline__ void produce_ring(const GemmParams &p, const CUtensor
                                              bool multicast, int rank, int cs, uint16_t mask,
                                              uint64_t policy, int unit0, int unit_stride,
                                              bool vocab, volatile int *abort_flag,
-                                             TileCoord (*coord)(const GemmParams &, int, int)) {
+                                             TileCoord (*coord)(const GemmParams &, int, int),
+                                             bool pair) {
+    // pair: the leader's barrier counts both CTAs' bytes; the peer's copies complete on the
+    // leader's barrier (at the same offset), and the peer's empty barriers are armed by the
+    // leader's MMA commits (cluster-scope acquire)
+    const bool peer = pair && rank == 1;
+    const bool leader = pair && rank == 0;
     int stage = 0;
     uint32_t phase = 0, issued = 0;
     bool ok = true;
@@ -522,13 +541,16 @@ __device__ __forceinline__ void produce_ring(const GemmParams &p, const CUtensor
         const TileCoord c = coord(p, tile, rank);
         const int row = is_a ? c.a_row : c.b_row;
         for (int kb = 0; kb < p.kblocks; ++kb) {
-            if (!bwait(&empty[stage], phase ^ 1u, abort_flag, p)) {
+            if (!(pair ? bwait_cl(&empty[stage], phase ^ 1u, abort_flag, p)
+                       : bwait(&empty[stage], phase ^ 1u, abort_flag, p))) {
                 ok = false;
                 break;
             }
-            mbar_arrive_expect_tx(&full[stage], stage_bytes);
+            if (!peer) mbar_arrive_expect_tx(&full[stage], leader ? 2 * stage_bytes : stage_bytes);
             uint8_t *dst = ring + stage * stage_bytes;
-            if (multicast)
+            if (peer)
+                tma_load_2d_pair(dst, tm, mapa_rank(&full[stage], 0), kb * kBlockK, row, policy);
+            else if (multicast)
                 tma_load_2d_mc(dst + rank * (stage_bytes / cs), tm, &full[stage], kb * kBlockK,
                                row, mask, policy);
             else
@@ -543,9 +565,22 @@ __device__ __forceinline__ void produce_ring(const GemmParams &p, const CUtensor
     // Drain: the last `stages` issues may still be landing (only possible after an abort;
     // on the normal path the MMA warp consumed every one of them).  A stage's barrier also
     // counts the bytes a cluster peer multicasts into it.
+    if (peer) {
+        // the peer cannot observe its copies (they complete on the leader's barrier); after
+        // an abort it gives the last ones a bounded time to land (they were issued at least
+        // one wait limit before an abort can happen, so this is normally already the case)
+        if (!ok) {
+            const uint64_t t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < 50000u) {
+            }
+        }
+        return;
+    }
+    // A pair leader's barrier also waits for the peer's bytes, which never come for a stage
+    // the peer did not issue: the drain stops at the first wait that runs out.
     const uint32_t n = issued < static_cast<uint32_t>(stages) ? issued : stages;
     for (uint32_t i = issued - n; i < issued; ++i)
-        bwait_drain(&full[i % stages], (i / stages) & 1u, abort_flag, p);
+        if (!bwait_drain(&full[i % stages], (i / stages) & 1u, abort_flag, p)) break;
 }
 
 template <bool VOCAB, int CS>
@@ -579,9 +614,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t b_stage_bytes = static_cast<uint32_t>(p.nb) * 128u;
-    // CTAs of a cluster walk the same work units in lockstep (same B-ring positions): the
-    // W share each loads is multicast into every peer's B stage.
+    // Rows mode with 2-CTA clusters, two schemes (kRowsPair):
+    //  - multicast: each CTA runs its own cta_group::1 MMA on the whole 256-row W tile, of
+    //    which it loads half and receives the other half by TMA multicast from its peer;
+    //  - pair: one cta_group::2 MMA (M = 256) per pair, issued by rank 0, with each CTA
+    //    staging only its half of the W tile (UMMA B split along N) and its own H tile (A
+    //    split along M); each CTA's TMEM holds its 128 rows.  The peer's copies complete on
+    //    the leader's stage barriers, which count both CTAs' bytes.
+    constexpr bool PAIR = !VOCAB && CS == 2 && kRowsPair;
+    const uint32_t b_stage_bytes = static_cast<uint32_t>(PAIR ? p.nb / 2 : p.nb) * 128u;
+    // CTAs of a cluster walk the same work units in lockstep (same ring positions).
     const int rank = CS > 1 ? static_cast<int>(cluster_ctarank()) : 0;
     const int unit0 = blockIdx.x / CS;
     const int unit_stride = gridDim.x / CS;
@@ -594,11 +636,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < p.stages_b; ++i) {
             mbar_init(&fullB[i], 1);
-            mbar_init(&emptyB[i], CS);  // one MMA commit from every CTA of the cluster
+            // multicast: one MMA commit from every CTA of the cluster; pair: the leader's
+            mbar_init(&emptyB[i], PAIR ? 1 : CS);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], kEpiWarps);
+            // pair: the leader's accumulator is free once both CTAs' epilogues are done
+            mbar_init(&tempty[i], PAIR ? 2 * kEpiWarps : kEpiWarps);
         }
         mbar_init(drain, 1);
         mbar_init(stall, 1);
@@ -621,8 +665,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (bad) atomicMax(p.ws.status, (static_cast<unsigned long long>(p.epoch) << 32) | 1ull);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, tmem_cols);
-        tmem_relinquish();
+        if (PAIR) {  // both CTAs' warps allocate together
+            tmem_alloc2(tmem_slot, tmem_cols);
+            tmem_relinquish2();
+        } else {
+            tmem_alloc(tmem_slot, tmem_cols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -643,17 +692,68 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          true, false, rank, CS, kClusterMask,
                                          VOCAB ? policy_evict_first() : policy_evict_last(),
                                          unit0, unit_stride, VOCAB, abort_flag,
-                                         coord_fn<VOCAB, CS>);
+                                         coord_fn<VOCAB, CS>, PAIR);
             else
                 produce_ring<kMaxStages>(p, &tmB, sB, b_stage_bytes, p.stages_b, fullB, emptyB,
-                                         false, CS > 1, rank, CS, kClusterMask,
+                                         false, CS > 1 && !PAIR, rank, CS, kClusterMask,
                                          VOCAB ? policy_evict_last() : policy_evict_normal(),
                                          unit0, unit_stride, VOCAB, abort_flag,
-                                         coord_fn<VOCAB, CS>);
+                                         coord_fn<VOCAB, CS>, PAIR);
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer (one lane)
-        if (lane == 0) {
+        if (PAIR && rank == 1) {
+            // pair peer: its copies complete on the leader's barriers; no MMA to issue
+        } else if (PAIR) {
+            // ------------------------------------------------ pair leader: one M = 256 MMA
+            // over both CTAs' stages per K step
+            if (lane == 0) {
+                const uint32_t idesc = idesc_bf16_f32(2 * kTileA, p.nb);
+                constexpr uint16_t kBoth = 3;
+                int sa = 0, sb = 0;
+                uint32_t pa = 0, pb = 0;
+                bool ok = true, any = false;
+                int it = 0;
+                for (int tile = unit0; ok && tile < p.num_tiles; tile += unit_stride, ++it) {
+                    const int b = it & 1;
+                    const uint32_t tph = (it >> 1) & 1;
+                    if (!bwait_cl(&tempty[b], tph ^ 1u, abort_flag, p)) break;
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * p.nb);
+                    for (int kb = 0; kb < p.kblocks; ++kb) {
+                        // the leader's barriers count both CTAs' bytes
+                        if (!bwait(&fullA[sa], pa, abort_flag, p) ||
+                            !bwait(&fullB[sb], pb, abort_flag, p)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + sa * kStageBytesA));
+                        const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + sb * b_stage_bytes));
+#pragma unroll
+                        for (int ks = 0; ks < kBlockK / 16; ++ks)
+                            umma_bf16_pair(d_tmem, adesc + 2u * ks, bdesc + 2u * ks, idesc,
+                                           (kb | ks) != 0 ? 1u : 0u);
+                        umma_commit_pair(&emptyA[sa], kBoth);  // frees the stage in both CTAs
+                        umma_commit_pair(&emptyB[sb], kBoth);
+                        any = true;
+                        if (++sa == p.stages_a) {
+                            sa = 0;
+                            pa ^= 1u;
+                        }
+                        if (++sb == p.stages_b) {
+                            sb = 0;
+                            pb ^= 1u;
+                        }
+                    }
+                    if (ok) umma_commit_pair(&tfull[b], kBoth);
+                }
+                if (any) {  // wait until every MMA this thread issued has completed
+                    umma_commit_pair(drain, 1);
+                    bwait_drain(drain, 0, abort_flag, p);
+                }
+            }
+        } else if (lane == 0) {
+            // ------------------------------------------------ MMA issuer (one lane)
             const uint32_t idesc = idesc_bf16_f32(kTileA, p.nb);
             int sa = 0, sb = 0;
             uint32_t pa = 0, pb = 0;
@@ -711,6 +811,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok;
             if (p.debug_stall)
                 ok = bwait(stall, 0, abort_flag, p);  // nothing ever arrives here
+            else if (PAIR)
+                ok = bwait_cl(&tfull[b], tph, abort_flag, p);  // the leader's commit
             else
                 ok = bwait(&tfull[b], tph, abort_flag, p);
             if (epi_vote_any(!ok)) break;
@@ -721,7 +823,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (VOCAB)
                 epilogue_vocab<EPI>(p, c, taddr, &tempty[b], q, h, lane, tgt_s, scratch);
             else
-                epilogue_rows<EPI>(p, c, taddr, &tempty[b], q, h, lane);
+                epilogue_rows<EPI>(p, c, taddr, &tempty[b], q, h, lane,
+                                   PAIR && rank == 1 ? mapa_rank(&tempty[b], 0) : 0u);
         }
     }
 
@@ -733,7 +836,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, tmem_cols);
+        if (PAIR)
+            tmem_dealloc2(tmem_base, tmem_cols);
+        else
+            tmem_dealloc(tmem_base, tmem_cols);
     }
 }
 

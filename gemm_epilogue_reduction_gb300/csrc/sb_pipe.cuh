@@ -44,15 +44,32 @@ __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, const Wait
     }
 }
 
+// bwait for a barrier whose arrivals come from another CTA of the cluster (cluster-scope
+// acquire).
+__device__ __forceinline__ bool bwait_cluster(uint64_t *bar, uint32_t parity, const WaitCtx w) {
+    if (mbar_test_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test_cluster(bar, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*w.abort_flag) return false;
+            if (globaltimer_ns() - t0 > w.timeout_ns) {
+                raise_timeout(w.status, w.epoch, w.abort_flag);
+                return false;
+            }
+        }
+    }
+}
+
 // Bounded wait used while draining: ignores the abort flag (the copies or MMAs being waited
-// for complete on their own), but still gives up after the time limit.
-__device__ __forceinline__ void bwait_drain(uint64_t *bar, uint32_t parity, const WaitCtx w) {
+// for complete on their own), but still gives up after the time limit; false then.
+__device__ __forceinline__ bool bwait_drain(uint64_t *bar, uint32_t parity, const WaitCtx w) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 0;; ++i) {
-        if (mbar_test(bar, parity)) return;
+        if (mbar_test(bar, parity)) return true;
         if ((i & 63u) == 63u && globaltimer_ns() - t0 > w.timeout_ns) {
             raise_timeout(w.status, w.epoch, w.abort_flag);
-            return;
+            return false;
         }
     }
 }

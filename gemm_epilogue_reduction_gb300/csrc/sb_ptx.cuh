@@ -70,6 +70,17 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         "r"(smem_u32(bar))
         : "memory");
 }
+// CTA-pair variant: the box lands in this CTA's shared memory and completes its bytes on
+// the mbarrier at cluster address `bar_cluster` (the pair leader's barrier).
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *tm,
+                                                 uint32_t bar_cluster, int32_t c0, int32_t c1,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".cta_group::2.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar_cluster), "r"(c0), "r"(c1), "l"(policy)
+        : "memory");
+}
 // Multicast variant: the box lands at the same shared-memory offset in every CTA of the
 // cluster named in cta_mask, and completes bytes on the mbarrier at the same offset in each.
 __device__ __forceinline__ void tma_load_2d_mc(void *dst, const CUtensorMap *tm, uint64_t *bar,
@@ -148,6 +159,67 @@ __device__ __forceinline__ void umma_commit_mc(uint64_t *bar, uint16_t cta_mask)
         " [%0], %1;" ::"r"(smem_u32(bar)),
         "h"(cta_mask)
         : "memory");
+}
+
+// ---------------------------------------------------------------- CTA pairs (cta_group::2)
+// One MMA for a pair of CTAs: one warp in each CTA allocates (collectively), the MMA is
+// issued from the pair's rank-0 CTA with A split along M and B along N across the two CTAs'
+// shared memory (same offsets), and each CTA's TMEM holds its half of the rows.  Every
+// tcgen05 instruction of a kernel uses the same CTA group.
+__device__ __forceinline__ void tmem_alloc2(uint32_t *dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish2() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrives once on the mbarrier at this offset in every CTA of cta_mask when all tcgen05
+// operations issued so far by this thread have completed.
+__device__ __forceinline__ void umma_commit_pair(uint64_t *bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+// Shared::cluster address of this CTA's shared variable `p` in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_rank(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+// One arrival, with release semantics at cluster scope, on an mbarrier of another CTA.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+// Probe with acquire semantics at cluster scope (arrivals from another CTA).
+__device__ __forceinline__ bool mbar_test_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
 }
 
 // ---------------------------------------------------------------- clusters
