@@ -91,8 +91,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # null once the source differs.
 KERNEL_TRAFFIC = {
     # decode16: dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
-    # (1,556,126,464 + 3,216,640 B; W + H are 1,555,988,480 B).
-    "decode16": {"bytes": 1559343104, "src_sha": "87ead7c27a97b079"},
+    # (1,556,143,360 + 3,161,088 B; W + H are 1,555,988,480 B).
+    "decode16": {"bytes": 1559304448, "src_sha": "9a3a32ccb902cc99"},
 }
 
 
