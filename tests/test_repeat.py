@@ -1,0 +1,67 @@
+"""Repeatability under load: the kernels have no data-dependent scheduling, so many calls in
+a row on the same inputs must return bit-identical outputs.  A race in the pipelines (a stage
+reused before its consumer finished, an accumulator overwritten before the epilogue read it,
+a CTA pair out of step) would show up as a call that differs."""
+import pytest
+import torch
+
+import gemm_epilogue_reduction_gb300 as sb
+from gemm_epilogue_reduction_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+@pytest.mark.parametrize("M,d,V,k,surface,calls", [
+    (512, 1024, 65536, 4, sb.SB_TOKEN_LOGPROB, 300),   # rows mode, CTA pairs, 2 M pairs
+    (300, 512, 32768, 2, sb.SB_GUMBEL_TOKEN, 300),     # rows mode, odd number of M tiles
+    (16, 1024, 151936, 4, sb.SB_TOKEN_LOGPROB, 300),   # vocab mode, decode shape
+    (64, 512, 65536, 2, sb.SB_FULL_LOGITS, 200),       # vocab mode, full logits
+])
+def test_many_calls_give_identical_bits(M, d, V, k, surface, calls):
+    H, W = synth.make_hw(M, d, V, seed=M + d, device="cuda")
+    out, bufs = sb.make_outputs(M, V, k, surface)
+    T = 0.8 if surface == sb.SB_GUMBEL_TOKEN else 1.0
+    keys = ["token", "token_logprob", "lse"] + (["logits"] if surface == sb.SB_FULL_LOGITS else [])
+
+    def call():
+        assert sb.sb_lmhead_project(H, W, M, d, V, k, surface, T, 99, out) == sb.SB_OK
+
+    call()
+    torch.cuda.synchronize()
+    first = {key: bufs[key].clone() for key in keys}
+    changed = []
+    for i in range(calls):
+        for key in keys:
+            bufs[key].fill_(0)
+        call()
+        if i % 25 == 24 or i == calls - 1:
+            torch.cuda.synchronize()
+            for key in keys:
+                if not torch.equal(bufs[key], first[key]):
+                    changed.append((i, key))
+    torch.cuda.synchronize()
+    assert sb.sb_last_device_status(out) == sb.SB_OK
+    assert not changed, changed[:5]
+
+
+def test_many_partial_completions_give_identical_bits():
+    M, N, K, lanes = 64, 2048, 8192, 2
+    X, W = synth.make_hw(M, K, N, seed=7, device="cuda")
+    nbytes = sb.sb_partial_workspace_bytes(M, N, K, lanes)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    Y = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    assert sb.sb_partial_completion(X, W, M, N, K, lanes, Y, False, ws, nbytes, None) == sb.SB_OK
+    torch.cuda.synchronize()
+    first = Y.clone()
+    for i in range(300):
+        Y.fill_(0)
+        assert sb.sb_partial_completion(X, W, M, N, K, lanes, Y, False, ws, nbytes, None) == sb.SB_OK
+        if i % 50 == 49:
+            torch.cuda.synchronize()
+            assert torch.equal(Y, first), i
