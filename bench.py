@@ -14,9 +14,10 @@ Prints one JSON line (rank 0):
               by its average duration, from K further launches of that kernel alone with
               CUDA events around each (sb_lmhead_records), against the measured HBM copy
               bandwidth (kernel timed alone: the burst figure);
-  e2e         the same metric through the public C-ABI call with host buffers: each step
-              copies H from pinned host memory, runs the call and reads back token and
-              log-prob, then waits for them;
+  e2e         the same metric through the public C-ABI call with host buffers
+              (sb_lmhead_project_from_host): each step the call copies H from pinned host
+              memory, runs the projection and copies token and log-prob back, and the step
+              waits for them;
   cpu_baseline  the fp64 oracle (plain C, OpenMP over the host cores) on a bounded sample of
               the same workload (rank 0, N = 1 only).
 ``--impl reference`` times that oracle alone as the reference arm.  With N > 1 (torchrun),
@@ -419,30 +420,28 @@ def main():
     torch.cuda.synchronize()
     comb_ms = [evk[2 * i].elapsed_time(evk[2 * i + 1]) for i in range(K)]
 
-    # ---- end to end through the public call, host buffers
-    # token and log-prob live side by side in one device buffer, read back with one copy
+    # ---- end to end through the public call with host buffers: H is copied from pinned
+    # host memory and token + log-prob are copied back inside the call, every step
     E = min(args.e2e_steps, K)
     H_host = H.cpu().pin_memory()
-    res_dev = torch.empty(2 * M, dtype=torch.int32, device="cuda")
-    res_host = torch.empty(2 * M, dtype=torch.int32).pin_memory()
-    e2e_out = sb.sb_outputs(res_dev.data_ptr(), res_dev.data_ptr() + 4 * M, out.lse,
-                            out.logits_bf16, out.target_ids, out.target_logprob, out.workspace,
-                            out.workspace_bytes, out.topk_ids, out.topk_logprob, out.topk)
+    tok_host = torch.empty(M, dtype=torch.int32).pin_memory()
+    lp_host = torch.empty(M, dtype=torch.float32).pin_memory()
     H_dev = torch.empty_like(H)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(E):
-        H_dev.copy_(H_host, non_blocking=True)
-        st = sb.sb_lmhead_project(H_dev, W, M, d, V, k, surface, T, gseed, e2e_out, stream)
+        st = sb.sb_lmhead_project_from_host(H_host, H_dev, W, M, d, V, k, surface, T, gseed,
+                                            out, tok_host, lp_host, stream)
         if st != sb.SB_OK:
-            raise sb.SbError(st, "sb_lmhead_project")
-        res_host.copy_(res_dev, non_blocking=True)
+            raise sb.SbError(st, "sb_lmhead_project_from_host")
         stream.synchronize()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / E
+    e2e_h2d = M * d * 2
+    e2e_d2h = 2 * M * 4
 
     ms_per_step = total_ms / K
     value = job_rows_per_s(world, M, ms_per_step)
@@ -491,7 +490,7 @@ def main():
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": {"value": M / (e2e_ms * 1e-3) * world, "unit": "rows/s",
-                    "h2d_bytes_per_step": M * d * 2, "d2h_bytes_per_step": M * 8,
+                    "h2d_bytes_per_step": e2e_h2d, "d2h_bytes_per_step": e2e_d2h,
                     "ms_per_step": e2e_ms},
             "clocks": clocks.summary(),
             "gpu_launches": 2 * K,

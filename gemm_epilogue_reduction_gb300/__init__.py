@@ -71,6 +71,10 @@ def lib():
         L.sb_lmhead_records.restype = i32
         L.sb_lmhead_project_static_scratch.argtypes = L.sb_lmhead_project.argtypes
         L.sb_lmhead_project_static_scratch.restype = i32
+        L.sb_lmhead_project_from_host.argtypes = [P, P, P, i64, i64, i64, i32, i32,
+                                                  ctypes.c_float, u64,
+                                                  ctypes.POINTER(sb_outputs), P, P, P]
+        L.sb_lmhead_project_from_host.restype = i32
         L.sb_combine_shard_records.argtypes = [P, i64, i32, i32, i32, ctypes.c_float,
                                                ctypes.POINTER(sb_outputs), P]
         L.sb_combine_shard_records.restype = i32
@@ -134,6 +138,17 @@ def sb_lmhead_project(H, W, M, d, V, k, surface, temperature, seed, out: sb_outp
     return int(lib().sb_lmhead_project(_ptr(H), _ptr(W), M, d, V, k, surface,
                                        float(temperature), seed & (2**64 - 1),
                                        ctypes.byref(out), _stream(stream)))
+
+
+def sb_lmhead_project_from_host(H_host, H_dev, W, M, d, V, k, surface, temperature, seed,
+                                out: sb_outputs, token_host, token_logprob_host=None,
+                                stream=None) -> int:
+    """H_host, token_host and token_logprob_host are host tensors (pinned for asynchronous
+    copies) or raw host addresses; H_dev and W are device tensors."""
+    return int(lib().sb_lmhead_project_from_host(
+        _ptr(H_host), _ptr(H_dev), _ptr(W), M, d, V, k, surface, float(temperature),
+        seed & (2**64 - 1), ctypes.byref(out), _ptr(token_host), _ptr(token_logprob_host),
+        _stream(stream)))
 
 
 def sb_lmhead_records(H, W, M, d, V, k, surface, temperature, seed, out: sb_outputs,

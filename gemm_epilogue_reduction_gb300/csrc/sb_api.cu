@@ -273,11 +273,20 @@ int32_t sb_tiles_per_shard(int64_t M, int64_t V, int32_t k) {
 
 namespace {
 
-// Validates, then enqueues the fused GEMM + record epilogue and, when `with_combine`, the
-// record combine.
-int32_t enqueue(const void *H, const void *W, int64_t M, int64_t d, int64_t V, int32_t k,
+// A validated call: kernel parameters and tensor maps, ready to enqueue.
+struct Prepared {
+    GemmParams p;
+    CUtensorMap tmA, tmB;
+    size_t smem;
+    int sms;
+    bool vm;
+    CombineParams c;
+};
+
+// Validates a call and builds its launch state; enqueues nothing.
+int32_t prepare(const void *H, const void *W, int64_t M, int64_t d, int64_t V, int32_t k,
                 int32_t surface, float temperature, uint64_t seed, const sb_outputs *out,
-                void *stream, bool with_combine) {
+                Prepared *pr) {
     if (!H || !W || !shape_ok(M, V, k) || d < 8 || d > (int64_t(1) << 24) ||
         surface < SB_TOKEN || surface > SB_TOPK_LOGPROB)
         return SB_ERR_INVALID_ARG;
@@ -298,7 +307,8 @@ int32_t enqueue(const void *H, const void *W, int64_t M, int64_t d, int64_t V, i
     const int flags = (gumbel ? kFlagGumbel : 0) | (surface == SB_FULL_LOGITS ? kFlagFull : 0) |
                       (out->target_ids ? kFlagTargets : 0) | (topk ? kFlagTopk : 0);
     const float inv_t = gumbel ? 1.0f / temperature : 1.0f;
-    GemmParams p{};
+    GemmParams &p = pr->p;
+    p = GemmParams{};
     p.M = static_cast<int>(M);
     p.d = static_cast<int>(d);
     p.V = static_cast<int>(V);
@@ -324,23 +334,39 @@ int32_t enqueue(const void *H, const void *W, int64_t M, int64_t d, int64_t V, i
     p.targets = out->target_ids;
     p.logits = out->logits_bf16;
     p.ws = ws_views(out->workspace, L, gumbel, K);
-    p.epoch = g_epoch.fetch_add(1) + 1;
     p.timeout_ns = g_timeout_ns.load();
     p.debug_stall = g_debug_stall.load();
 
-    CUtensorMap tmA, tmB;
     // rows mode: each CTA of a cluster loads 256 / cluster rows of the shared W tile
-    const bool ok = vm ? (make_map(&tmA, W, V, d, kTileA) && make_map(&tmB, H, M, d, p.nb))
-                       : (make_map(&tmA, H, M, d, kTileA) &&
-                          make_map(&tmB, W, V, d, kRowsTileN / p.cluster));
+    const bool ok = vm ? (make_map(&pr->tmA, W, V, d, kTileA) && make_map(&pr->tmB, H, M, d, p.nb))
+                       : (make_map(&pr->tmA, H, M, d, kTileA) &&
+                          make_map(&pr->tmB, W, V, d, kRowsTileN / p.cluster));
     if (!ok) return SB_ERR_CUDA;
-    const size_t smem = lmhead_smem_bytes(p.nb, p.stages_a, p.stages_b, vm, flags, K);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (launch_lmhead(vm, tmA, tmB, p, smem, dev.sms, st) != cudaSuccess) return SB_ERR_CUDA;
-    if (!with_combine) return SB_OK;
-    const CombineParams c = combine_params(out, p.ws, M, k, T, flags, inv_t);
-    if (launch_combine(c, st) != cudaSuccess) return SB_ERR_CUDA;
+    pr->smem = lmhead_smem_bytes(p.nb, p.stages_a, p.stages_b, vm, flags, K);
+    pr->sms = dev.sms;
+    pr->vm = vm;
+    pr->c = combine_params(out, p.ws, M, k, T, flags, inv_t);
     return SB_OK;
+}
+
+// Enqueues a prepared call: the fused GEMM + record epilogue and, when `with_combine`, the
+// record combine.  Each launch gets a new epoch.
+int32_t launch(Prepared &pr, void *stream, bool with_combine) {
+    pr.p.epoch = g_epoch.fetch_add(1) + 1;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (launch_lmhead(pr.vm, pr.tmA, pr.tmB, pr.p, pr.smem, pr.sms, st) != cudaSuccess)
+        return SB_ERR_CUDA;
+    if (!with_combine) return SB_OK;
+    if (launch_combine(pr.c, st) != cudaSuccess) return SB_ERR_CUDA;
+    return SB_OK;
+}
+
+int32_t enqueue(const void *H, const void *W, int64_t M, int64_t d, int64_t V, int32_t k,
+                int32_t surface, float temperature, uint64_t seed, const sb_outputs *out,
+                void *stream, bool with_combine) {
+    Prepared pr;
+    if (int32_t e = prepare(H, W, M, d, V, k, surface, temperature, seed, out, &pr)) return e;
+    return launch(pr, stream, with_combine);
 }
 
 }  // namespace
@@ -357,6 +383,30 @@ int32_t sb_lmhead_records(const void *H, const void *W, int64_t M, int64_t d, in
                           int32_t k, int32_t surface, float temperature, uint64_t seed,
                           const sb_outputs *out, void *stream) {
     return enqueue(H, W, M, d, V, k, surface, temperature, seed, out, stream, false);
+}
+
+int32_t sb_lmhead_project_from_host(const void *H_host, void *H_dev, const void *W, int64_t M,
+                                    int64_t d, int64_t V, int32_t k, int32_t surface,
+                                    float temperature, uint64_t seed, const sb_outputs *out,
+                                    int32_t *token_host, float *token_logprob_host,
+                                    void *stream) {
+    if (!H_host || !token_host) return SB_ERR_INVALID_ARG;
+    Prepared pr;
+    if (int32_t e = prepare(H_dev, W, M, d, V, k, surface, temperature, seed, out, &pr)) return e;
+    if (token_logprob_host && !out->token_logprob) return SB_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(H_dev, H_host, static_cast<size_t>(M) * d * 2, cudaMemcpyHostToDevice,
+                        st) != cudaSuccess)
+        return SB_ERR_CUDA;
+    if (int32_t e = launch(pr, stream, true)) return e;
+    if (cudaMemcpyAsync(token_host, out->token, static_cast<size_t>(M) * 4,
+                        cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return SB_ERR_CUDA;
+    if (token_logprob_host &&
+        cudaMemcpyAsync(token_logprob_host, out->token_logprob, static_cast<size_t>(M) * 4,
+                        cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return SB_ERR_CUDA;
+    return SB_OK;
 }
 
 int32_t sb_combine_shard_records(const void *workspace, int64_t M, int32_t k,

@@ -174,6 +174,27 @@ int32_t sb_lmhead_records(const void *H, const void *W, int64_t M, int64_t d, in
                           const sb_outputs *out, void *stream);
 
 /*
+ * sb_lmhead_project for a caller whose hidden states are in host memory and who wants the
+ * token surface back in host memory ("SemBridge", Section 5.2: the consumer observes the
+ * projected surface, never the logits).  Enqueues on stream, in order: one copy of H_host
+ * into H_dev, the projection of sb_lmhead_project on H_dev, and one copy each of out->token
+ * into token_host and (when token_logprob_host is not NULL) of out->token_logprob into
+ * token_logprob_host.
+ *   H_host              host bf16 [M, d]; pinned memory makes the copy asynchronous.
+ *   H_dev               device staging buffer of M * d bf16, 16-byte aligned; overwritten.
+ *   out                 device outputs and workspace as for sb_lmhead_project.
+ *   token_host          host int32 [M] (required); token_logprob_host host float [M] or NULL
+ *                       (then out->token_logprob may be NULL); pinned for asynchronous copies.
+ * The caller synchronises stream before reading the host outputs.  Every argument is checked
+ * before anything is enqueued; returns an sb_status.
+ */
+int32_t sb_lmhead_project_from_host(const void *H_host, void *H_dev, const void *W, int64_t M,
+                                    int64_t d, int64_t V, int32_t k, int32_t surface,
+                                    float temperature, uint64_t seed, const sb_outputs *out,
+                                    int32_t *token_host, float *token_logprob_host,
+                                    void *stream);
+
+/*
  * The record combine alone (the second kernel of sb_lmhead_project): reads the per-tile
  * records of `workspace` (layout above; tiles_per_shard = T) and writes token,
  * token_logprob, lse and target_logprob of `out` (those that are non-NULL).  Per row it

@@ -117,3 +117,11 @@ def test_valid_arguments_without_a_gpu_report_a_device_error():
     st = sb.sb_lmhead_project(0x30000000, 0x40000000, 4, 256, 4096, 2, sb.SB_TOKEN, 1.0, 0,
                               out, 0)
     assert st in (sb.SB_ERR_CUDA, sb.SB_ERR_UNSUPPORTED)
+
+
+def test_host_buffer_entry_rejects_missing_host_buffers_before_any_copy():
+    out = _outputs()
+    for h_host, tok_host in ((0, 0x7000), (0x7000, 0)):
+        st = sb.sb_lmhead_project_from_host(h_host, 0x30000000, 0x40000000, 4, 256, 4096, 2,
+                                            sb.SB_TOKEN, 1.0, 0, out, tok_host, None, 0)
+        assert st == sb.SB_ERR_INVALID_ARG

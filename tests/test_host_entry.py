@@ -1,0 +1,45 @@
+"""sb_lmhead_project_from_host: the projection with host-memory hidden states and host-memory
+token outputs gives exactly the bits of sb_lmhead_project on the same inputs, for pinned and
+for pageable host buffers."""
+import pytest
+import torch
+
+import gemm_epilogue_reduction_gb300 as sb
+from gemm_epilogue_reduction_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+@pytest.mark.parametrize("M,d,V,k,surface", [
+    (16, 512, 40000, 4, sb.SB_TOKEN_LOGPROB),
+    (300, 256, 12000, 3, sb.SB_GUMBEL_TOKEN),
+    (5, 64, 1000, 1, sb.SB_TOKEN),
+])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_buffer_call_matches_the_device_call(M, d, V, k, surface, pinned):
+    H, W = synth.make_hw(M, d, V, seed=M + V, device="cuda")
+    T = 0.9 if surface == sb.SB_GUMBEL_TOKEN else 1.0
+    ref = sb.project(H, W, k, surface, temperature=T, seed=3)
+    H_host = H.cpu()
+    tok_host = torch.full((M,), -1, dtype=torch.int32)
+    lp_host = torch.full((M,), float("nan"), dtype=torch.float32)
+    if pinned:
+        H_host, tok_host, lp_host = H_host.pin_memory(), tok_host.pin_memory(), lp_host.pin_memory()
+    H_dev = torch.empty_like(H)
+    out, bufs = sb.make_outputs(M, V, k, surface)
+    want_lp = surface != sb.SB_TOKEN
+    st = sb.sb_lmhead_project_from_host(H_host, H_dev, W, M, d, V, k, surface, T, 3, out,
+                                        tok_host, lp_host if want_lp else None)
+    assert st == sb.SB_OK
+    torch.cuda.synchronize()
+    assert sb.sb_last_device_status(out) == sb.SB_OK
+    assert torch.equal(H_dev, H)
+    assert torch.equal(tok_host, ref["token"].cpu())
+    if want_lp:
+        assert torch.equal(lp_host, ref["token_logprob"].cpu())
