@@ -74,6 +74,8 @@ __global__ void __launch_bounds__(32 * kMaxWarps) combine_kernel(const CombinePa
     const int row = blockIdx.x;
     // Launched as a programmatic dependent of the GEMM: wait until that grid has completed
     // and its record writes are visible.
+    // let the next kernel in the stream (a dependent launch) start its setup early
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int sh_i = warp; sh_i < p.k; sh_i += nwarps) {
         Rec r{-INFINITY, INT_MAX, 0.f};
@@ -162,6 +164,8 @@ __global__ void __launch_bounds__(32 * kMaxWarps) pack_kernel(const PayloadParam
     const int warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
     const int row = blockIdx.x;
+    // let the next kernel in the stream (a dependent launch) start its setup early
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int sh_i = warp; sh_i < p.k; sh_i += nwarps) {
         Rec r{-INFINITY, INT_MAX, 0.f};
@@ -222,6 +226,8 @@ __global__ void __launch_bounds__(32 * kMaxWarps) pack_kernel(const PayloadParam
 template <bool GUMBEL>
 __global__ void merge_payload_kernel(const CombineParams c, const unsigned char *payload) {
     const int row = blockIdx.x * blockDim.x + threadIdx.x;
+    // let the next kernel in the stream (a dependent launch) start its setup early
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (row >= c.M) return;
     Rec acc{-INFINITY, INT_MAX, 0.f};
@@ -348,6 +354,8 @@ __global__ void __launch_bounds__(32 * kMaxWarps) combine_topk_kernel(const Comb
     const int nwarps = blockDim.x >> 5;
     const int nthreads = blockDim.x;
     const int row = blockIdx.x;
+    // let the next kernel in the stream (a dependent launch) start its setup early
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // 1. shard records (the plain combine's tree)

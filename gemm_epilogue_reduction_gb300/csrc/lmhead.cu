@@ -650,19 +650,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        if (blockIdx.x == 0) *p.ws.epoch = p.epoch;
-    }
-    if (VOCAB && (p.flags & kFlagTargets))
-        for (int i = threadIdx.x; i < p.M; i += blockDim.x) tgt_s[i] = p.targets[i];
-    // Scoring targets outside [0, V) would leave their log-prob undefined: CTA 0 checks them
-    // and reports SB_ERR_INVALID_ARG through the status word (the outputs stay undefined).
-    if (blockIdx.x == 0 && (p.flags & kFlagTargets)) {
-        bool bad = false;
-        for (int i = threadIdx.x; i < p.M; i += blockDim.x) {
-            const int t = p.targets[i];
-            bad |= (t < 0 || t >= p.V);
-        }
-        if (bad) atomicMax(p.ws.status, (static_cast<unsigned long long>(p.epoch) << 32) | 1ull);
     }
     if (warp == 1) {
         if (PAIR) {  // both CTAs' warps allocate together
@@ -678,6 +665,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (CS > 1) cluster_sync();  // peers' barriers are initialised before any multicast
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // The setup above touches no global memory, so it overlaps the previous kernel in the
+    // stream (this kernel is a programmatic dependent launch); the inputs and the workspace
+    // may belong to that kernel, so everything from here on waits for it.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (blockIdx.x == 0 && threadIdx.x == 0) *p.ws.epoch = p.epoch;
+    if (VOCAB && (p.flags & kFlagTargets))
+        for (int i = threadIdx.x; i < p.M; i += blockDim.x) tgt_s[i] = p.targets[i];
+    // Scoring targets outside [0, V) would leave their log-prob undefined: CTA 0 checks them
+    // and reports SB_ERR_INVALID_ARG through the status word (the outputs stay undefined).
+    if (blockIdx.x == 0 && (p.flags & kFlagTargets)) {
+        bool bad = false;
+        for (int i = threadIdx.x; i < p.M; i += blockDim.x) {
+            const int t = p.targets[i];
+            bad |= (t < 0 || t >= p.V);
+        }
+        if (bad) atomicMax(p.ws.status, (static_cast<unsigned long long>(p.epoch) << 32) | 1ull);
+    }
+    if (VOCAB && (p.flags & kFlagTargets)) __syncthreads();  // tgt_s is complete
     // Let the record combine (a programmatic dependent launch) get scheduled early; it
     // waits for this whole grid to finish before it reads any record.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -868,13 +873,17 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmP
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // a programmatic dependent of the previous kernel in the stream: its CTAs may start
+    // their setup early and wait (griddepcontrol.wait) before touching global memory
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     // persistent grid: as many clusters as can be resident at once (one CTA per SM)
     int clusters = num_sms / CS;
     if (CS > 1) {

@@ -128,7 +128,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
         fence_mbar_init();
         tma_prefetch_desc(&tmW);
         tma_prefetch_desc(&tmX);
-        if (blockIdx.x == 0) *p.epoch_word = p.epoch;
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, tmem_cols);
@@ -138,6 +137,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // The setup above touches no global memory, so it overlaps the previous kernel in the
+    // stream (this kernel is a programmatic dependent launch); X, W and the workspace may
+    // belong to that kernel, so everything from here on waits for it.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (blockIdx.x == 0 && threadIdx.x == 0) *p.epoch_word = p.epoch;
     // let the completion (a programmatic dependent launch) get scheduled early; it waits for
     // this whole grid before it reads any slab
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -273,6 +277,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
 __global__ void __launch_bounds__(256)
     complete_kernel(const PartialParams p) {
     constexpr int kBatch = 8;
+    // let the next kernel in the stream (a dependent launch) start its setup early
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const size_t items = static_cast<size_t>(p.n_tiles) * p.M * (kTileA / 4);
     for (size_t it = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; it < items;
@@ -442,8 +448,21 @@ int32_t sb_partial_completion(const void *X, const void *W, int64_t M, int64_t N
     uint32_t cols = 32;
     while (cols < static_cast<uint32_t>(2 * p.nb)) cols <<= 1;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    partial_kernel<<<p.grid, kPThreads, smem, st>>>(tmW, tmX, p, cols);
-    if (cudaGetLastError() != cudaSuccess) return SB_ERR_CUDA;
+    {
+        // a programmatic dependent of the previous kernel in the stream (see the kernel)
+        cudaLaunchConfig_t pc{};
+        pc.gridDim = dim3(static_cast<unsigned>(p.grid));
+        pc.blockDim = dim3(kPThreads);
+        pc.dynamicSmemBytes = smem;
+        pc.stream = st;
+        cudaLaunchAttribute pa[1];
+        pa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        pa[0].val.programmaticStreamSerializationAllowed = 1;
+        pc.attrs = pa;
+        pc.numAttrs = 1;
+        if (cudaLaunchKernelEx(&pc, partial_kernel, tmW, tmX, p, cols) != cudaSuccess)
+            return SB_ERR_CUDA;
+    }
 
     int sms = 0, cc = 0;
     if (int32_t e = device_sms_cc(&sms, &cc)) return e;
