@@ -422,10 +422,15 @@ def main():
 
     # ---- end to end through the public call with host buffers: H is copied from pinned
     # host memory and token + log-prob are copied back inside the call, every step
+    # (token and log-prob back to back on both sides, so they come back in one copy)
     E = min(args.e2e_steps, K)
     H_host = H.cpu().pin_memory()
-    tok_host = torch.empty(M, dtype=torch.int32).pin_memory()
-    lp_host = torch.empty(M, dtype=torch.float32).pin_memory()
+    res_host = torch.empty(2 * M, dtype=torch.int32).pin_memory()
+    tok_host, lp_host = res_host[:M], res_host[M:].view(torch.float32)
+    res_dev = torch.empty(2 * M, dtype=torch.int32, device="cuda")
+    e2e_out = sb.sb_outputs(res_dev.data_ptr(), res_dev.data_ptr() + 4 * M, out.lse,
+                            out.logits_bf16, out.target_ids, out.target_logprob, out.workspace,
+                            out.workspace_bytes, out.topk_ids, out.topk_logprob, out.topk)
     H_dev = torch.empty_like(H)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -433,7 +438,7 @@ def main():
     e0.record(stream)
     for _ in range(E):
         st = sb.sb_lmhead_project_from_host(H_host, H_dev, W, M, d, V, k, surface, T, gseed,
-                                            out, tok_host, lp_host, stream)
+                                            e2e_out, tok_host, lp_host, stream)
         if st != sb.SB_OK:
             raise sb.SbError(st, "sb_lmhead_project_from_host")
         stream.synchronize()

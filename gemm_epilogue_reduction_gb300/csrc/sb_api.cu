@@ -399,12 +399,20 @@ int32_t sb_lmhead_project_from_host(const void *H_host, void *H_dev, const void 
                         st) != cudaSuccess)
         return SB_ERR_CUDA;
     if (int32_t e = launch(pr, stream, true)) return e;
-    if (cudaMemcpyAsync(token_host, out->token, static_cast<size_t>(M) * 4,
-                        cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    // token and log-prob stored back to back on both sides: one copy
+    const size_t n = static_cast<size_t>(M) * 4;
+    const bool joined =
+        token_logprob_host &&
+        reinterpret_cast<const char *>(out->token_logprob) ==
+            reinterpret_cast<const char *>(out->token) + n &&
+        reinterpret_cast<const char *>(token_logprob_host) ==
+            reinterpret_cast<const char *>(token_host) + n;
+    if (cudaMemcpyAsync(token_host, out->token, joined ? 2 * n : n, cudaMemcpyDeviceToHost,
+                        st) != cudaSuccess)
         return SB_ERR_CUDA;
-    if (token_logprob_host &&
-        cudaMemcpyAsync(token_logprob_host, out->token_logprob, static_cast<size_t>(M) * 4,
-                        cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    if (token_logprob_host && !joined &&
+        cudaMemcpyAsync(token_logprob_host, out->token_logprob, n, cudaMemcpyDeviceToHost,
+                        st) != cudaSuccess)
         return SB_ERR_CUDA;
     return SB_OK;
 }

@@ -185,8 +185,10 @@ int32_t sb_lmhead_records(const void *H, const void *W, int64_t M, int64_t d, in
  *   out                 device outputs and workspace as for sb_lmhead_project.
  *   token_host          host int32 [M] (required); token_logprob_host host float [M] or NULL
  *                       (then out->token_logprob may be NULL); pinned for asynchronous copies.
- * The caller synchronises stream before reading the host outputs.  Every argument is checked
- * before anything is enqueued; returns an sb_status.
+ * When out->token_logprob directly follows out->token (M int32) and token_logprob_host
+ * directly follows token_host, both come back in one copy.  The caller synchronises stream
+ * before reading the host outputs.  Every argument is checked before anything is enqueued;
+ * returns an sb_status.
  */
 int32_t sb_lmhead_project_from_host(const void *H_host, void *H_dev, const void *W, int64_t M,
                                     int64_t d, int64_t V, int32_t k, int32_t surface,

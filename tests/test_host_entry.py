@@ -43,3 +43,22 @@ def test_host_buffer_call_matches_the_device_call(M, d, V, k, surface, pinned):
     assert torch.equal(tok_host, ref["token"].cpu())
     if want_lp:
         assert torch.equal(lp_host, ref["token_logprob"].cpu())
+
+
+def test_host_buffer_call_with_token_and_logprob_back_to_back():
+    """Device and host buffers laid out as [token | log-prob]: one copy brings both back."""
+    M, d, V, k = 16, 512, 40000, 4
+    H, W = synth.make_hw(M, d, V, seed=9, device="cuda")
+    ref = sb.project(H, W, k, sb.SB_TOKEN_LOGPROB)
+    res_dev = torch.empty(2 * M, dtype=torch.int32, device="cuda")
+    res_host = torch.full((2 * M,), -1, dtype=torch.int32).pin_memory()
+    out, bufs = sb.make_outputs(M, V, k, sb.SB_TOKEN_LOGPROB)
+    out.token, out.token_logprob = res_dev.data_ptr(), res_dev.data_ptr() + 4 * M
+    H_dev = torch.empty_like(H)
+    st = sb.sb_lmhead_project_from_host(H.cpu().pin_memory(), H_dev, W, M, d, V, k,
+                                        sb.SB_TOKEN_LOGPROB, 1.0, 0, out, res_host[:M],
+                                        res_host[M:].view(torch.float32))
+    assert st == sb.SB_OK
+    torch.cuda.synchronize()
+    assert torch.equal(res_host[:M], ref["token"].cpu())
+    assert torch.equal(res_host[M:].view(torch.float32), ref["token_logprob"].cpu())
