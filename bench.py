@@ -92,8 +92,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # null once the source differs.
 KERNEL_TRAFFIC = {
     # decode16: dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
-    # (1,556,143,360 + 3,161,088 B; W + H are 1,555,988,480 B).
-    "decode16": {"bytes": 1559304448, "src_sha": "9a3a32ccb902cc99"},
+    # (1,556,226,304 + 3,238,400 B; W + H are 1,555,988,480 B).
+    "decode16": {"bytes": 1559464704, "src_sha": "c2f44351b44b2eb3"},
 }
 
 
