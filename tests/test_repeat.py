@@ -22,6 +22,7 @@ def _built():
     (300, 512, 32768, 2, sb.SB_GUMBEL_TOKEN, 300),     # rows mode, odd number of M tiles
     (16, 1024, 151936, 4, sb.SB_TOKEN_LOGPROB, 300),   # vocab mode, decode shape
     (64, 512, 65536, 2, sb.SB_FULL_LOGITS, 200),       # vocab mode, full logits
+    (4096, 6144, 200064, 4, sb.SB_TOKEN_LOGPROB, 20),  # the prefill shape, 16 M pairs
 ])
 def test_many_calls_give_identical_bits(M, d, V, k, surface, calls):
     H, W = synth.make_hw(M, d, V, seed=M + d, device="cuda")
