@@ -10,8 +10,10 @@
 // m, s = sum_C exp(y - m).  The merge of two records keeps the larger max, the lower index
 // on an equal max, and rescales both sums to the new max.  It is commutative bit for bit;
 // its associativity holds only up to rounding, so the order is fixed:
-//   per (row, shard): lane l of one warp folds tiles l, l+32, ... in ascending order, then
-//                     an xor butterfly (16, 8, 4, 2, 1) merges the 32 lane results;
+//   per (row, shard): lane l of one warp takes tiles l, l+32, ..., l+480 of each batch of 512
+//                     and folds them as a balanced pairwise tree (adjacent pairs, four
+//                     levels), folds the batch results in ascending order, then an xor
+//                     butterfly (16, 8, 4, 2, 1) merges the 32 lane results;
 //   per row:          the k shard results merge in ascending shard order.
 // One block serves one row; its warps take the shards round-robin.
 // The output bits are therefore a function of the record bits alone (any grid, any run).
@@ -56,9 +58,67 @@ __device__ __forceinline__ GRec gmerge(const GRec &a, const GRec &b) {
 constexpr int kMaxWarps = 8;
 constexpr int kBatch = 16;  // records each lane loads before folding them
 
-// One block per row; warp w completes shards w, w + 8, ... (lane l folds tiles l, l+32, ...
-// in ascending order, loading kBatch of them at a time, then the xor butterfly), writes the
-// shard record to shared memory, and thread 0 merges the k shard records in ascending order.
+// Pairwise tree over x[0 .. N): adjacent pairs first, the result in x[0].
+template <int N, typename R, typename F>
+__device__ __forceinline__ void tree_fold(R (&x)[N], F f) {
+#pragma unroll
+    for (int w = 1; w < N; w *= 2)
+#pragma unroll
+        for (int u = 0; u + w < N; u += 2 * w) x[u] = f(x[u], x[u + w]);
+}
+
+// Shard-local completion of (row, shard) by one warp in the fixed order above; every lane
+// returns the shard record (and the Gumbel record).  on_rec(t, rec) sees each of the lane's
+// records (t < T) as it is loaded, in ascending tile order.
+template <bool GUMBEL, typename OnRec>
+__device__ __forceinline__ void shard_fold(const Workspace &ws, size_t base, int T, int lane,
+                                           Rec &r, GRec &g, OnRec on_rec) {
+    r = Rec{-INFINITY, INT_MAX, 0.f};
+    g = GRec{-INFINITY, INT_MAX, 0.f};
+    for (int t0 = lane; t0 < T; t0 += 32 * kBatch) {
+        Rec x[kBatch];
+        GRec y[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int t = t0 + 32 * u;
+            if (t < T) {
+                x[u] = Rec{__ldg(ws.m + base + t), __ldg(ws.idx + base + t),
+                           __ldg(ws.s + base + t)};
+                if (GUMBEL)
+                    y[u] = GRec{__ldg(ws.gk + base + t), __ldg(ws.gi + base + t),
+                                __ldg(ws.gz + base + t)};
+            } else {
+                x[u] = Rec{-INFINITY, INT_MAX, 0.f};
+                if (GUMBEL) y[u] = GRec{-INFINITY, INT_MAX, 0.f};
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+            if (t0 + 32 * u < T) on_rec(t0 + 32 * u, x[u]);
+        tree_fold(x, [](const Rec &a, const Rec &b) { return merge(a, b); });
+        r = merge(r, x[0]);
+        if (GUMBEL) {
+            tree_fold(y, [](const GRec &a, const GRec &b) { return gmerge(a, b); });
+            g = gmerge(g, y[0]);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const Rec o{__shfl_xor_sync(0xFFFFFFFFu, r.m, off),
+                    __shfl_xor_sync(0xFFFFFFFFu, r.i, off),
+                    __shfl_xor_sync(0xFFFFFFFFu, r.s, off)};
+        r = merge(r, o);
+        if (GUMBEL) {
+            const GRec go{__shfl_xor_sync(0xFFFFFFFFu, g.k, off),
+                          __shfl_xor_sync(0xFFFFFFFFu, g.i, off),
+                          __shfl_xor_sync(0xFFFFFFFFu, g.z, off)};
+            g = gmerge(g, go);
+        }
+    }
+}
+
+// One block per row; warp w completes shards w, w + 8, ... (shard_fold), writes the shard
+// record to shared memory, and thread 0 merges the k shard records in ascending order.
 template <bool GUMBEL>
 __global__ void __launch_bounds__(32 * kMaxWarps) combine_kernel(const CombineParams p) {
     extern __shared__ float sh[];  // k records: m, i, s [, gk, gi, gz]
@@ -78,45 +138,10 @@ __global__ void __launch_bounds__(32 * kMaxWarps) combine_kernel(const CombinePa
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int sh_i = warp; sh_i < p.k; sh_i += nwarps) {
-        Rec r{-INFINITY, INT_MAX, 0.f};
-        GRec g{-INFINITY, INT_MAX, 0.f};
-        const size_t base = (static_cast<size_t>(row) * p.k + sh_i) * p.T;
-        for (int t0 = lane; t0 < p.T; t0 += 32 * kBatch) {
-            Rec x[kBatch];
-            GRec y[kBatch];
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int t = t0 + 32 * u;
-                if (t < p.T) {
-                    x[u] = Rec{__ldg(p.ws.m + base + t), __ldg(p.ws.idx + base + t),
-                               __ldg(p.ws.s + base + t)};
-                    if (GUMBEL)
-                        y[u] = GRec{__ldg(p.ws.gk + base + t), __ldg(p.ws.gi + base + t),
-                                    __ldg(p.ws.gz + base + t)};
-                } else {
-                    x[u] = Rec{-INFINITY, INT_MAX, 0.f};
-                    if (GUMBEL) y[u] = GRec{-INFINITY, INT_MAX, 0.f};
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                r = merge(r, x[u]);
-                if (GUMBEL) g = gmerge(g, y[u]);
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const Rec o{__shfl_xor_sync(0xFFFFFFFFu, r.m, off),
-                        __shfl_xor_sync(0xFFFFFFFFu, r.i, off),
-                        __shfl_xor_sync(0xFFFFFFFFu, r.s, off)};
-            r = merge(r, o);
-            if (GUMBEL) {
-                const GRec go{__shfl_xor_sync(0xFFFFFFFFu, g.k, off),
-                              __shfl_xor_sync(0xFFFFFFFFu, g.i, off),
-                              __shfl_xor_sync(0xFFFFFFFFu, g.z, off)};
-                g = gmerge(g, go);
-            }
-        }
+        Rec r;
+        GRec g;
+        shard_fold<GUMBEL>(p.ws, (static_cast<size_t>(row) * p.k + sh_i) * p.T, p.T, lane, r, g,
+                           [](int, const Rec &) {});
         if (lane == 0) {
             sm[sh_i] = r.m;
             si[sh_i] = r.i;
@@ -168,45 +193,10 @@ __global__ void __launch_bounds__(32 * kMaxWarps) pack_kernel(const PayloadParam
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int sh_i = warp; sh_i < p.k; sh_i += nwarps) {
-        Rec r{-INFINITY, INT_MAX, 0.f};
-        GRec g{-INFINITY, INT_MAX, 0.f};
-        const size_t base = (static_cast<size_t>(row) * p.k + sh_i) * p.T;
-        for (int t0 = lane; t0 < p.T; t0 += 32 * kBatch) {
-            Rec x[kBatch];
-            GRec y[kBatch];
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int t = t0 + 32 * u;
-                if (t < p.T) {
-                    x[u] = Rec{__ldg(p.ws.m + base + t), __ldg(p.ws.idx + base + t),
-                               __ldg(p.ws.s + base + t)};
-                    if (GUMBEL)
-                        y[u] = GRec{__ldg(p.ws.gk + base + t), __ldg(p.ws.gi + base + t),
-                                    __ldg(p.ws.gz + base + t)};
-                } else {
-                    x[u] = Rec{-INFINITY, INT_MAX, 0.f};
-                    if (GUMBEL) y[u] = GRec{-INFINITY, INT_MAX, 0.f};
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                r = merge(r, x[u]);
-                if (GUMBEL) g = gmerge(g, y[u]);
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const Rec o{__shfl_xor_sync(0xFFFFFFFFu, r.m, off),
-                        __shfl_xor_sync(0xFFFFFFFFu, r.i, off),
-                        __shfl_xor_sync(0xFFFFFFFFu, r.s, off)};
-            r = merge(r, o);
-            if (GUMBEL) {
-                const GRec go{__shfl_xor_sync(0xFFFFFFFFu, g.k, off),
-                              __shfl_xor_sync(0xFFFFFFFFu, g.i, off),
-                              __shfl_xor_sync(0xFFFFFFFFu, g.z, off)};
-                g = gmerge(g, go);
-            }
-        }
+        Rec r;
+        GRec g;
+        shard_fold<GUMBEL>(p.ws, (static_cast<size_t>(row) * p.k + sh_i) * p.T, p.T, lane, r, g,
+                           [](int, const Rec &) {});
         if (lane == 0) {
             const size_t rec = static_cast<size_t>(sh_i) * p.M + row;
             float *f = reinterpret_cast<float *>(p.payload + rec * (GUMBEL ? 24 : 12));
@@ -254,9 +244,10 @@ __device__ __forceinline__ float unord_f(uint32_t o) {
     return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
 }
 
-// K rounds of warp max over the lanes' sorted lists (tv, ti) of kMaxTopK entries; lane 0
+// K rounds of warp max over the lanes' sorted lists (tv, ti) of KL entries; lane 0
 // writes the winners to (ov, oi).  Lanes with nothing hold (-inf, INT_MAX) heads.
-__device__ __forceinline__ void warp_select(const float (&tv)[kMaxTopK], const int (&ti)[kMaxTopK],
+template <int KL>
+__device__ __forceinline__ void warp_select(const float (&tv)[KL], const int (&ti)[KL],
                                             int K, float *ov, int *oi) {
     const int lane = threadIdx.x & 31;
     int hp = 0;
@@ -264,7 +255,7 @@ __device__ __forceinline__ void warp_select(const float (&tv)[kMaxTopK], const i
         float hv = -INFINITY;
         int hi = INT_MAX;
 #pragma unroll
-        for (int e = 0; e < kMaxTopK; ++e)
+        for (int e = 0; e < KL; ++e)
             if (e == hp) {
                 hv = tv[e];
                 hi = ti[e];
@@ -272,7 +263,7 @@ __device__ __forceinline__ void warp_select(const float (&tv)[kMaxTopK], const i
         const uint32_t oh = ord_f(hv);
         const uint32_t om = __reduce_max_sync(0xFFFFFFFFu, oh);
         const int wi = __reduce_min_sync(0xFFFFFFFFu, oh == om ? hi : INT_MAX);
-        if (oh == om && hi == wi && hp < kMaxTopK) ++hp;
+        if (oh == om && hi == wi && hp < KL) ++hp;
         if (lane == 0) {
             ov[q] = unord_f(om);
             oi[q] = wi;
@@ -280,13 +271,14 @@ __device__ __forceinline__ void warp_select(const float (&tv)[kMaxTopK], const i
     }
 }
 
-__device__ __forceinline__ void list_insert(float (&tv)[kMaxTopK], int (&ti)[kMaxTopK], float x,
+template <int KL>
+__device__ __forceinline__ void list_insert(float (&tv)[KL], int (&ti)[KL], float x,
                                             int xi) {
     float cv = x;
     int ci = xi;
     bool ins = false;
 #pragma unroll
-    for (int q = 0; q < kMaxTopK; ++q) {
+    for (int q = 0; q < KL; ++q) {
         if (ins || cv > tv[q]) {
             const float a = tv[q];
             const int b = ti[q];
@@ -299,15 +291,10 @@ __device__ __forceinline__ void list_insert(float (&tv)[kMaxTopK], int (&ti)[kMa
     }
 }
 
-// Rank of (v, i) against (tv, ti) in the surface's order (larger value first, then lower
-// column): true if (v, i) ranks at or above.
-__device__ __forceinline__ bool ranks_at_or_above(float v, int i, float tv, int ti) {
-    return v > tv || (v == tv && i <= ti);
-}
-
 // Block-wide top-K of the threads' sorted lists: each warp picks its K best, then warp 0
 // picks the K best of the warps' lists into (ov, oi) in shared memory.
-__device__ __forceinline__ void block_select(const float (&tv)[kMaxTopK], const int (&ti)[kMaxTopK],
+template <int KL>
+__device__ __forceinline__ void block_select(const float (&tv)[KL], const int (&ti)[KL],
                                              int K, float *wlv, int *wli, float *ov, int *oi) {
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -315,10 +302,10 @@ __device__ __forceinline__ void block_select(const float (&tv)[kMaxTopK], const 
     warp_select(tv, ti, K, wlv + warp * K, wli + warp * K);
     __syncthreads();
     if (warp == 0) {
-        float lv[kMaxTopK];
-        int li[kMaxTopK];
+        float lv[KL];
+        int li[KL];
 #pragma unroll
-        for (int q = 0; q < kMaxTopK; ++q) {
+        for (int q = 0; q < KL; ++q) {
             const bool have = lane < nwarps && q < K;
             lv[q] = have ? wlv[lane * K + q] : -INFINITY;
             li[q] = have ? wli[lane * K + q] : INT_MAX;
@@ -328,19 +315,43 @@ __device__ __forceinline__ void block_select(const float (&tv)[kMaxTopK], const 
     __syncthreads();
 }
 
+// Rank-aware insertion for entries that arrive in no particular column order: (x, xi) goes
+// before the first entry it ranks above (larger value, or an equal value at a lower column).
+template <int KL>
+__device__ __forceinline__ void list_insert_ranked(float (&tv)[KL], int (&ti)[KL],
+                                                   float x, int xi) {
+    float cv = x;
+    int ci = xi;
+    bool ins = false;
+#pragma unroll
+    for (int q = 0; q < KL; ++q) {
+        if (ins || cv > tv[q] || (cv == tv[q] && ci < ti[q])) {
+            const float a = tv[q];
+            const int b = ti[q];
+            tv[q] = cv;
+            ti[q] = ci;
+            cv = a;
+            ci = b;
+            ins = true;
+        }
+    }
+}
+
 // Top-K combine, one block per row.
 //  1. lse and token: exactly the fixed tree of the plain combine (so they equal the token
 //     surface's bits): warps over shards, lanes over tiles, xor butterfly, shards ascending.
-//  2. theta = the K-th largest of the row's tile maxima.  The K tiles whose maxima rank at
-//     or above theta hold K distinct entries that do, so no entry ranking below theta can
-//     be in the row's top K.
-//  3. Only records whose maximum ranks at or above theta are read; their entries ranking
-//     at or above theta are the candidates, and the block selects the K best of them.
-// Each thread walks its records in ascending column order, so an equal value already in
-// its list has the lower column (list_insert keeps it first).  Selection compares values
-// only, so the result does not depend on how the work is split.
+//     The same loads feed each lane's list of its best tile maxima, keyed by record number
+//     (records are numbered in ascending column order, so the lower record number is the
+//     lower column on an equal maximum).
+//  2. The block selects the K records with the best maxima.  Every entry of the row's top K
+//     lies in one of them: an entry of any other record has K distinct entries (those K
+//     maxima) ranking above it.
+//  3. One warp reads those K records' sorted lists (K x K entries) and selects the K best.
+// Selection compares (value, column) only, so the result does not depend on how the work is
+// split.
+template <int KL>
 __global__ void __launch_bounds__(32 * kMaxWarps) combine_topk_kernel(const CombineParams p) {
-    extern __shared__ float sh[];  // k x (m, i, s); 8 x K warp lists; 2 x K block lists; theta
+    extern __shared__ float sh[];  // k x (m, i, s); 8 x K warp lists; 2 x K block lists
     const int K = p.topk;
     float *sm = sh;
     int *si = reinterpret_cast<int *>(sh + p.k);
@@ -352,35 +363,28 @@ __global__ void __launch_bounds__(32 * kMaxWarps) combine_topk_kernel(const Comb
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
-    const int nthreads = blockDim.x;
     const int row = blockIdx.x;
+    const int nrec = p.k * p.T;
+    const size_t rbase = static_cast<size_t>(row) * nrec;
     // let the next kernel in the stream (a dependent launch) start its setup early
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // 1. shard records (the plain combine's tree)
+    // 1. shard records (the plain combine's tree) and the lanes' best maxima
+    float tv[KL];
+    int ti[KL];
+#pragma unroll
+    for (int q = 0; q < KL; ++q) {
+        tv[q] = -INFINITY;
+        ti[q] = INT_MAX;
+    }
     for (int sh_i = warp; sh_i < p.k; sh_i += nwarps) {
-        Rec r{-INFINITY, INT_MAX, 0.f};
-        const size_t base = (static_cast<size_t>(row) * p.k + sh_i) * p.T;
-        for (int t0 = lane; t0 < p.T; t0 += 32 * kBatch) {
-            Rec x[kBatch];
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int t = t0 + 32 * u;
-                x[u] = t < p.T ? Rec{__ldg(p.ws.m + base + t), __ldg(p.ws.idx + base + t),
-                                     __ldg(p.ws.s + base + t)}
-                               : Rec{-INFINITY, INT_MAX, 0.f};
-            }
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) r = merge(r, x[u]);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const Rec o{__shfl_xor_sync(0xFFFFFFFFu, r.m, off),
-                        __shfl_xor_sync(0xFFFFFFFFu, r.i, off),
-                        __shfl_xor_sync(0xFFFFFFFFu, r.s, off)};
-            r = merge(r, o);
-        }
+        Rec r;
+        GRec g;
+        const int fbase = sh_i * p.T;
+        shard_fold<false>(p.ws, rbase + fbase, p.T, lane, r, g, [&](int t, const Rec &x) {
+            if (x.m > tv[KL - 1]) list_insert(tv, ti, x.m, fbase + t);
+        });
         if (lane == 0) {
             sm[sh_i] = r.m;
             si[sh_i] = r.i;
@@ -388,62 +392,48 @@ __global__ void __launch_bounds__(32 * kMaxWarps) combine_topk_kernel(const Comb
         }
     }
 
-    // 2. theta from the tile maxima (a row's records are contiguous: f = s * T + t)
-    const int nrec = p.k * p.T;
-    const size_t rbase = static_cast<size_t>(row) * nrec;
-    float tv[kMaxTopK];
-    int ti[kMaxTopK];
+    // 2. the K records with the best maxima (record numbers in bli; INT_MAX past the row's
+    //    records when it has fewer than K)
+    block_select(tv, ti, K, wlv, wli, blv, bli);
+    if (warp != 0) return;
+
+    // 3. the K best of those records' lists
 #pragma unroll
-    for (int q = 0; q < kMaxTopK; ++q) {
+    for (int q = 0; q < KL; ++q) {
         tv[q] = -INFINITY;
         ti[q] = INT_MAX;
     }
-    for (int f = threadIdx.x; f < nrec; f += nthreads) {
-        const float m = __ldg(p.ws.m + rbase + f);
-        if (m > tv[kMaxTopK - 1]) list_insert(tv, ti, m, __ldg(p.ws.idx + rbase + f));
+    constexpr int kPer = (KL * KL + 31) / 32;  // entries per lane at the largest K
+    float xv[kPer];
+    int xi[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int j = lane + 32 * u;
+        const int f = j < K * K ? bli[min(j / K, K - 1)] : INT_MAX;
+        const bool have = f < nrec;
+        const size_t o = have ? (rbase + f) * K + j % K : 0;
+        xv[u] = have ? __ldg(p.ws.tkv + o) : -INFINITY;
+        xi[u] = have ? __ldg(p.ws.tki + o) : INT_MAX;
     }
-    block_select(tv, ti, K, wlv, wli, blv, bli);
-    const float th_v = blv[K - 1];  // -inf / INT_MAX when the row has fewer than K tiles
-    const int th_i = bli[K - 1];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u)
+        if (xv[u] != -INFINITY) list_insert_ranked(tv, ti, xv[u], xi[u]);
+    __syncwarp();
+    warp_select(tv, ti, K, wlv, wli);  // warp 0's slot of the warp lists is free again
+    __syncwarp();
 
-    // 3. candidates at or above theta
-#pragma unroll
-    for (int q = 0; q < kMaxTopK; ++q) {
-        tv[q] = -INFINITY;
-        ti[q] = INT_MAX;
-    }
-    for (int f = threadIdx.x; f < nrec; f += nthreads) {
-        const float m = __ldg(p.ws.m + rbase + f);
-        const int mi = __ldg(p.ws.idx + rbase + f);
-        if (!ranks_at_or_above(m, mi, th_v, th_i) && th_v != -INFINITY) continue;
-        const size_t o = (rbase + f) * K;
-        float xv[kMaxTopK];
-        int xi[kMaxTopK];
-#pragma unroll
-        for (int e = 0; e < kMaxTopK; ++e) {
-            xv[e] = e < K ? __ldg(p.ws.tkv + o + e) : -INFINITY;
-            xi[e] = e < K ? __ldg(p.ws.tki + o + e) : INT_MAX;
-        }
-#pragma unroll
-        for (int e = 0; e < kMaxTopK; ++e)
-            if (xv[e] > tv[kMaxTopK - 1] &&
-                (th_v == -INFINITY || ranks_at_or_above(xv[e], xi[e], th_v, th_i)))
-                list_insert(tv, ti, xv[e], xi[e]);
-    }
-    block_select(tv, ti, K, wlv, wli, blv, bli);
-
-    if (threadIdx.x != 0) return;
     Rec acc{-INFINITY, INT_MAX, 0.f};
     for (int s2 = 0; s2 < p.k; ++s2) acc = merge(acc, Rec{sm[s2], si[s2], ss[s2]});
     const float lse = acc.m + logf(acc.s);
+    if (lane < K) {
+        p.topk_ids[static_cast<size_t>(row) * K + lane] = wli[lane];
+        p.topk_logprob[static_cast<size_t>(row) * K + lane] = wlv[lane] - lse;
+    }
+    if (lane != 0) return;
     p.token[row] = acc.i;
     if (p.lse) p.lse[row] = lse;
     if (p.token_logprob) p.token_logprob[row] = -logf(acc.s);
     if (p.target_logprob) p.target_logprob[row] = p.ws.tz[row] - lse;
-    for (int q = 0; q < K; ++q) {
-        p.topk_ids[static_cast<size_t>(row) * K + q] = bli[q];
-        p.topk_logprob[static_cast<size_t>(row) * K + q] = blv[q] - lse;
-    }
 }
 
 }  // namespace
@@ -464,7 +454,10 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
         cfg.blockDim = dim3(32 * kMaxWarps);
         cfg.dynamicSmemBytes = static_cast<size_t>(p.k) * 12 +
                                static_cast<size_t>(kMaxWarps + 1) * 8 * p.topk;
-        return cudaLaunchKernelEx(&cfg, combine_topk_kernel, p);
+        // lists sized to the smallest of 4, 8, 16 entries that holds K
+        if (p.topk <= 4) return cudaLaunchKernelEx(&cfg, combine_topk_kernel<4>, p);
+        if (p.topk <= 8) return cudaLaunchKernelEx(&cfg, combine_topk_kernel<8>, p);
+        return cudaLaunchKernelEx(&cfg, combine_topk_kernel<kMaxTopK>, p);
     }
     if (p.flags & kFlagGumbel) return cudaLaunchKernelEx(&cfg, combine_kernel<true>, p);
     return cudaLaunchKernelEx(&cfg, combine_kernel<false>, p);

@@ -74,8 +74,10 @@ __host__ __device__ inline SmemLayout make_layout(int nb, int stages_a, int stag
     off += vocab ? kMaxVocabModeRows * 4 : 0;
     L.scratch_off = off;
     off += vocab ? 4 * nb * ((flags & kFlagGumbel) ? 24 : 12) : 0;
-    // top-K: the quadrants' lists, values then columns
-    off += (vocab && (flags & kFlagTopk)) ? 4 * nb * topk * 8 : 0;
+    // top-K: the tile's logits, nb rows of 128 fp32 (16-byte aligned: everything before it
+    // is a multiple of 16 bytes)
+    off += (vocab && (flags & kFlagTopk)) ? nb * kVocabTileV * 4 : 0;
+    (void)topk;
     L.total = off + 1024;  // slack to align the base to 1024 bytes
     return L;
 }
@@ -164,6 +166,18 @@ __device__ __forceinline__ uint16_t bf16_bits_rn(float z) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(z));
 }
 
+// Compare-exchange for a descending sort of (key, position) pairs: after it, (ka, ea) ranks
+// at or above (kb, eb), i.e. the larger key, or the lower position on an equal key.
+__device__ __forceinline__ void cas_desc(uint32_t &ka, int &ea, uint32_t &kb, int &eb) {
+    const bool swap = kb > ka || (kb == ka && eb < ea);
+    const uint32_t k = swap ? kb : ka;
+    const int e = swap ? eb : ea;
+    kb = swap ? ka : kb;
+    eb = swap ? ea : eb;
+    ka = k;
+    ea = e;
+}
+
 // ------------------------------------------------------------------ epilogue, vocab mode
 // Thread (warp quadrant q, lane) holds vocabulary column v = v0 + 32q + lane for every row
 // (TMEM columns).  The two warps of a quadrant take alternate 8-row chunks (half h takes
@@ -180,7 +194,8 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
     constexpr bool TOPK = EPI == kEpiTopk;
     const int nb = p.nb;
     const int K = p.topk;
-    const int v = c.v0 + 32 * q + lane;
+    const int col0 = c.v0 + 32 * q;  // column of lane 0: lanes hold ascending columns
+    const int v = col0 + lane;
     const bool valid = v < c.v_end;
     const bool has_t = (p.flags & kFlagTargets) != 0;
     float *sc_m = scratch;
@@ -189,79 +204,83 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
     float *sc_gk = scratch + 12 * nb;
     int *sc_gi = reinterpret_cast<int *>(scratch + 16 * nb);
     float *sc_gz = scratch + 20 * nb;
-    // top-K scratch: [quadrant][row][K] values, then the same for columns
-    float *sc_tv = scratch + 12 * nb;
-    int *sc_ti = reinterpret_cast<int *>(sc_tv + 4 * nb * K);
+    float *zs = scratch + 12 * nb;  // top-K: the tile's logits, [row][128]
 
-    // nb is a multiple of 16, so every chunk is 8 whole accumulator columns
+    // nb is a multiple of 16, so every chunk is 8 whole accumulator columns.  The chunk's
+    // rows are independent, so each step is issued for all 8 rows before the next step (the
+    // warp reductions of different rows overlap); rows past M (zero rows of H) go through
+    // the reductions and are not stored.
     for (int c0 = 8 * h; c0 < nb; c0 += 16) {
-        uint32_t raw[8];
         constexpr int cw = 8;
+        uint32_t raw[cw];
         tmem_ld32x32b_x8(taddr + c0, raw);
-        float my_m = -INFINITY, my_s = 0.f, my_gk = -INFINITY, my_gz = 0.f;
-        int my_i = INT_MAX, my_gi = INT_MAX;
-        // stream index of (row c0 + j, column v) is (c0 + j) V + v: the state advances by
-        // V golden-ratio increments per row
-        unsigned long long st = 0ull;
-        if (GUMBEL)
-            st = splitmix_state(p.seed, static_cast<unsigned long long>(c0) *
-                                                static_cast<unsigned>(p.V) +
-                                            static_cast<unsigned>(v));
-        float my_tv[TOPK ? kMaxTopK : 1];
-        int my_ti[TOPK ? kMaxTopK : 1];
+        float y[cw];
+        uint32_t oy[cw], om[cw];
 #pragma unroll
         for (int j = 0; j < cw; ++j) {
-            const int row = c0 + j;
-            if (row >= p.M) break;
             const float z = __uint_as_float(raw[j]);
-            const float y = valid ? (GUMBEL ? z * p.inv_t : z) : -INFINITY;
-            const uint32_t oy = float_to_ordered(y);
-            const uint32_t om = __reduce_max_sync(0xFFFFFFFFu, oy);
-            const float wm = ordered_to_float(om);
-            const int wi = __reduce_min_sync(0xFFFFFFFFu, (valid && oy == om) ? v : INT_MAX);
-            float ws = valid ? ex2_approx(fmaf(y, kLog2e, -wm * kLog2e)) : 0.f;
+            y[j] = valid ? (GUMBEL ? z * p.inv_t : z) : -INFINITY;
+            oy[j] = float_to_ordered(y[j]);
+        }
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) ws += __shfl_xor_sync(0xFFFFFFFFu, ws, off);
-            if (GUMBEL) {
+        for (int j = 0; j < cw; ++j) om[j] = __reduce_max_sync(0xFFFFFFFFu, oy[j]);
+        int wi[cw];
+        float ws[cw];
+#pragma unroll
+        for (int j = 0; j < cw; ++j) {
+            wi[j] = __reduce_min_sync(0xFFFFFFFFu, (valid && oy[j] == om[j]) ? v : INT_MAX);
+            const float wm = ordered_to_float(om[j]);
+            ws[j] = valid ? ex2_approx(fmaf(y[j], kLog2e, -wm * kLog2e)) : 0.f;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int j = 0; j < cw; ++j) ws[j] += __shfl_xor_sync(0xFFFFFFFFu, ws[j], off);
+        float my_m = -INFINITY, my_s = 0.f, my_gk = -INFINITY, my_gz = 0.f;
+        int my_i = INT_MAX, my_gi = INT_MAX;
+#pragma unroll
+        for (int j = 0; j < cw; ++j)
+            if (lane == j) {
+                my_m = ordered_to_float(om[j]);
+                my_i = wi[j];
+                my_s = ws[j];
+            }
+        if (GUMBEL) {
+            // stream index of (row c0 + j, column v) is (c0 + j) V + v: the state advances by
+            // V golden-ratio increments per row
+            unsigned long long st = splitmix_state(
+                p.seed, static_cast<unsigned long long>(c0) * static_cast<unsigned>(p.V) +
+                            static_cast<unsigned>(v));
+            uint32_t ok[cw], okm[cw];
+#pragma unroll
+            for (int j = 0; j < cw; ++j) {
                 const float g = gumbel_from_bits(bits24_from_state(st));
                 st += static_cast<unsigned long long>(static_cast<unsigned>(p.V)) * kGolden;
-                const float key = valid ? y + g : -INFINITY;
-                const uint32_t ok = float_to_ordered(key);
-                const uint32_t okm = __reduce_max_sync(0xFFFFFFFFu, ok);
-                const int gi = __reduce_min_sync(0xFFFFFFFFu, (valid && ok == okm) ? v : INT_MAX);
-                const int src = (gi == INT_MAX) ? 0 : (gi - (c.v0 + 32 * q));
-                const float gz = __shfl_sync(0xFFFFFFFFu, z, src & 31);
+                ok[j] = float_to_ordered(valid ? y[j] + g : -INFINITY);
+            }
+#pragma unroll
+            for (int j = 0; j < cw; ++j) okm[j] = __reduce_max_sync(0xFFFFFFFFu, ok[j]);
+#pragma unroll
+            for (int j = 0; j < cw; ++j) {
+                const int gi =
+                    __reduce_min_sync(0xFFFFFFFFu, (valid && ok[j] == okm[j]) ? v : INT_MAX);
+                const int src = (gi == INT_MAX) ? 0 : (gi - col0);
+                const float gz = __shfl_sync(0xFFFFFFFFu, __uint_as_float(raw[j]), src & 31);
                 if (lane == j) {
-                    my_gk = ordered_to_float(okm);
+                    my_gk = ordered_to_float(okm[j]);
                     my_gi = gi;
                     my_gz = gz;
                 }
             }
-            if (TOPK) {
-                // the quadrant's K largest of this row: K rounds of warp max (lowest column
-                // on ties), each removing its winner
-                bool alive = valid;
+        }
 #pragma unroll
-                for (int r = 0; r < kMaxTopK; ++r) {
-                    if (r >= K) break;
-                    const uint32_t oc = alive ? oy : float_to_ordered(-INFINITY);
-                    const uint32_t ocm = __reduce_max_sync(0xFFFFFFFFu, oc);
-                    const int ci =
-                        __reduce_min_sync(0xFFFFFFFFu, (alive && oc == ocm) ? v : INT_MAX);
-                    if (v == ci) alive = false;
-                    if (lane == j) {
-                        my_tv[r] = ordered_to_float(ocm);
-                        my_ti[r] = ci;
-                    }
-                }
-            }
-            if (FULL && valid) p.logits[static_cast<size_t>(row) * p.V + v] = bf16_bits_rn(z);
-            if (has_t && valid && tgt_s[row] == v) p.ws.tz[row] = z;
-            if (lane == j) {
-                my_m = wm;
-                my_i = wi;
-                my_s = ws;
-            }
+        for (int j = 0; j < cw; ++j) {
+            const int row = c0 + j;
+            if (row >= p.M || !valid) continue;
+            const float z = __uint_as_float(raw[j]);
+            if (FULL) p.logits[static_cast<size_t>(row) * p.V + v] = bf16_bits_rn(z);
+            if (has_t && tgt_s[row] == v) p.ws.tz[row] = z;
+            if (TOPK) zs[row * kVocabTileV + 32 * q + lane] = z;
         }
         if (lane < cw && c0 + lane < p.M) {
             const int o = q * nb + c0 + lane;
@@ -272,14 +291,6 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
                 sc_gk[o] = my_gk;
                 sc_gi[o] = my_gi;
                 sc_gz[o] = my_gz;
-            }
-            if (TOPK) {
-#pragma unroll
-                for (int r = 0; r < kMaxTopK; ++r) {
-                    if (r >= K) break;
-                    sc_tv[o * K + r] = my_tv[r];
-                    sc_ti[o * K + r] = my_ti[r];
-                }
             }
         }
     }
@@ -325,30 +336,89 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
             p.ws.gi[ri] = gi;
             p.ws.gz[ri] = gz;
         }
-        if (TOPK) {  // merge the four quadrants' sorted lists into the tile's top K
-            int p0 = 0, p1 = 0, p2 = 0, p3 = 0;
-            for (int r = 0; r < K; ++r) {
-                float bv = -INFINITY;
-                int bi = INT_MAX, bw = -1;
+    }
+    if (TOPK) {
+        // the record's K largest per row over the whole 128-column tile.  Warp e of the
+        // epilogue takes rows e, e + 8, ... two at a time; lane l holds columns 4l .. 4l + 3,
+        // sorted (larger first, lower column on ties).  Each round the warp max of the lanes'
+        // heads wins; the lowest lane holding it has the lowest column, writes the entry to
+        // shared memory (over the row's logits, already in registers) and drops its head.
+        // Key 0 (below every ordered float) marks an empty slot; an entry no round fills
+        // stays (-inf, INT_MAX).  The lists leave in one coalesced store per row.
+        const int nvalid = c.v_end - c.v0;
+        const int ew = (threadIdx.x >> 5) - kFirstEpiWarp;
+        const uint32_t lt = lanemask_lt();
+        const int c4 = 4 * lane;
+        for (int r0 = ew; r0 < p.M; r0 += 2 * kEpiWarps) {
+            uint32_t k0[2], k1[2], k2[2], k3[2];
+            int e0[2], e1[2], e2[2], e3[2];
+            float *lv[2];
+            int *li[2];
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const int pw = w == 0 ? p0 : (w == 1 ? p1 : (w == 2 ? p2 : p3));
-                    if (pw >= K) continue;
-                    const int o = (w * nb + row) * K + pw;
-                    const float vw = sc_tv[o];
-                    const int iw = sc_ti[o];
-                    if (vw > bv || (vw == bv && iw < bi)) {
-                        bv = vw;
-                        bi = iw;
-                        bw = w;
-                    }
+            for (int u = 0; u < 2; ++u) {
+                const int row = r0 + u * kEpiWarps;
+                const bool have = row < p.M;
+                float *zr = zs + (have ? row : r0) * kVocabTileV;
+                const float4 x = *reinterpret_cast<const float4 *>(zr + c4);
+                k0[u] = have && c4 + 0 < nvalid ? float_to_ordered(x.x) : 0u;
+                k1[u] = have && c4 + 1 < nvalid ? float_to_ordered(x.y) : 0u;
+                k2[u] = have && c4 + 2 < nvalid ? float_to_ordered(x.z) : 0u;
+                k3[u] = have && c4 + 3 < nvalid ? float_to_ordered(x.w) : 0u;
+                e0[u] = 0;
+                e1[u] = 1;
+                e2[u] = 2;
+                e3[u] = 3;
+                cas_desc(k0[u], e0[u], k1[u], e1[u]);
+                cas_desc(k2[u], e2[u], k3[u], e3[u]);
+                cas_desc(k0[u], e0[u], k2[u], e2[u]);
+                cas_desc(k1[u], e1[u], k3[u], e3[u]);
+                cas_desc(k1[u], e1[u], k2[u], e2[u]);
+                // the list goes over the row's first 2K logits (a missing second row reuses
+                // the first row's slots at offset 64: it is never read back)
+                lv[u] = zr + (have ? 0 : 64);
+                li[u] = reinterpret_cast<int *>(lv[u] + kMaxTopK);
+            }
+            __syncwarp();  // every lane has read its logits before the lists overwrite them
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                if (lane < K) {
+                    lv[u][lane] = -INFINITY;
+                    li[u][lane] = INT_MAX;
                 }
-                p0 += bw == 0;
-                p1 += bw == 1;
-                p2 += bw == 2;
-                p3 += bw == 3;
-                p.ws.tkv[ri * K + r] = bv;
-                p.ws.tki[ri * K + r] = bi;
+            __syncwarp();
+#pragma unroll
+            for (int r = 0; r < kMaxTopK; ++r) {
+                if (r >= K) break;
+                uint32_t m[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) m[u] = __reduce_max_sync(0xFFFFFFFFu, k0[u]);
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const bool cand = m[u] != 0u && k0[u] == m[u];
+                    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, cand);
+                    const bool pop = cand && (hit & lt) == 0u;
+                    if (pop) {
+                        lv[u][r] = ordered_to_float(m[u]);
+                        li[u][r] = c.v0 + c4 + e0[u];
+                    }
+                    k0[u] = pop ? k1[u] : k0[u];
+                    e0[u] = pop ? e1[u] : e0[u];
+                    k1[u] = pop ? k2[u] : k1[u];
+                    e1[u] = pop ? e2[u] : e1[u];
+                    k2[u] = pop ? k3[u] : k2[u];
+                    e2[u] = pop ? e3[u] : e2[u];
+                    k3[u] = pop ? 0u : k3[u];
+                }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int row = r0 + u * kEpiWarps;
+                if (lane < K && row < p.M) {
+                    const size_t o = ((static_cast<size_t>(row) * p.k + c.s) * p.T + c.t) * K;
+                    p.ws.tkv[o + lane] = lv[u][lane];
+                    p.ws.tki[o + lane] = li[u][lane];
+                }
             }
         }
     }

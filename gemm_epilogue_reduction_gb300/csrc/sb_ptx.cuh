@@ -304,6 +304,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 // Monotone map float -> uint32 (ascending floats give ascending integers; no NaNs).
+// Mask of the lanes below this one in the warp.
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
 __device__ __forceinline__ uint32_t float_to_ordered(float f) {
     uint32_t u = __float_as_uint(f);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
