@@ -86,14 +86,17 @@ WORKLOADS = {
 }
 METRIC = "LM-head+projection rows/s; % of HBM GB/s (decode) or bf16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# nominal GB300 figures, reported beside the measured-peak fraction: ~8 TB/s HBM3e and
+# 2.25 PFLOP/s dense bf16
+NOMINAL_PEAKS = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0}
 
 # DRAM traffic of the GEMM kernel per launch from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), with the hash of the kernel source it was taken on; reported as
 # null once the source differs.
 KERNEL_TRAFFIC = {
     # decode16: dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
-    # (1,556,226,304 + 3,238,400 B; W + H are 1,555,988,480 B).
-    "decode16": {"bytes": 1559464704, "src_sha": "c2f44351b44b2eb3"},
+    # (1,556,263,168 + 3,237,888 B; W + H are 1,555,988,480 B).
+    "decode16": {"bytes": 1559501056, "src_sha": "4b7fd1e55bcd873b"},
 }
 
 
@@ -309,7 +312,9 @@ def run_partial(args, cfg, world, rank, local):
         "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": ach / peaks["hbm_gbs"], "traffic": None,
                      "peak_source": f"{peak_src} (HBM copy, burst)",
-                     "kernel": "partial_kernel + complete_kernel", "algorithmic_bytes": alg},
+                     "kernel": "partial_kernel + complete_kernel", "algorithmic_bytes": alg,
+                     "nominal": {"peak": NOMINAL_PEAKS["hbm_gbs"],
+                                 "frac": ach / NOMINAL_PEAKS["hbm_gbs"]}},
         "cpu_baseline": None, "e2e": None, "clocks": clocks.summary(), "gpu_launches": 2 * K_,
     }
     if rank == 0:
@@ -465,13 +470,17 @@ def main():
                 "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
                 "peak_source": f"{peak_src} (HBM copy, burst)", "kernel": "lmhead_kernel",
                 "kernel_ms": gemm_avg, "combine_ms": comb_avg,
-                "algorithmic_bytes": alg_bytes, "tensor_tflops": achieved_tfs}
+                "algorithmic_bytes": alg_bytes, "tensor_tflops": achieved_tfs,
+                "nominal": {"peak": NOMINAL_PEAKS["hbm_gbs"],
+                            "frac": achieved_gbs / NOMINAL_PEAKS["hbm_gbs"]}}
     else:
         roof = {"bound": "tensor", "achieved": achieved_tfs, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": achieved_tfs / peaks["bf16_tflops"], "traffic": traffic,
                 "peak_source": f"{peak_src} (cuBLAS bf16, burst)", "kernel": "lmhead_kernel",
                 "kernel_ms": gemm_avg, "combine_ms": comb_avg, "algorithmic_flops": alg_flops,
-                "hbm_gbs": achieved_gbs}
+                "hbm_gbs": achieved_gbs,
+                "nominal": {"peak": NOMINAL_PEAKS["bf16_tflops"],
+                            "frac": achieved_tfs / NOMINAL_PEAKS["bf16_tflops"]}}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
