@@ -83,6 +83,22 @@ def test_topk_ties_list_lower_columns_first(M):
     assert bool((lp == lp[0]).all())
 
 
+@pytest.mark.parametrize("M,k", [(4, 4), (300, 2)])
+def test_topk_more_ties_than_k_keep_the_lowest_columns(M, k):
+    """Six bit-identical maxima in five records and up to four shards, K = 4: the list is the
+    four lowest columns (the combine ranks records by maximum, then by record number, which
+    is column order)."""
+    d, V, K = 64, 2048, 4
+    H, W = synth.make_hw(M, d, V, seed=4)
+    W = W.clone()
+    W[1500] = (H[0].float() * 6.0 / d).to(torch.bfloat16)
+    W = synth.duplicate_rows(W, [(1500, c) for c in (1999, 701, 700, 300, 100)])
+    res = sb.project(H.cuda(), W.cuda(), k, sb.SB_TOPK_LOGPROB, topk=K)
+    torch.cuda.synchronize()
+    assert res["topk_ids"][0].tolist() == [100, 300, 700, 701]
+    assert int(res["token"][0]) == 100
+
+
 def test_topk_decode_shape():
     """The decode token-only shape (M=16, d=5120, V=151936, k=4) with K = 8."""
     M, d, V, k, K = 16, 5120, 151936, 4, 8
