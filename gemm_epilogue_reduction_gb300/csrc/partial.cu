@@ -138,8 +138,26 @@ __global__ void __launch_bounds__(kPThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     // The setup above touches no global memory, so it overlaps the previous kernel in the
-    // stream (this kernel is a programmatic dependent launch); X, W and the workspace may
-    // belong to that kernel, so everything from here on waits for it.
+    // stream (this kernel is a programmatic dependent launch).  W is a weight that kernel
+    // does not write, so ring W's first stages are filled before the wait (the W stream
+    // starts while the previous kernel finishes); X and the workspace may belong to that
+    // kernel, so everything else waits for it.
+    uint32_t w_pre = 0;
+    if (warp == 0 && lane == 0) {
+        const uint32_t n = x_end - x_begin;
+        w_pre = n < static_cast<uint32_t>(p.stages_w) ? n : static_cast<uint32_t>(p.stages_w);
+        int tile = static_cast<int>(x_begin / p.kb_tile);
+        int kb = static_cast<int>(x_begin) - tile * p.kb_tile;
+        const uint64_t pol = policy_evict_first();
+        for (uint32_t i = 0; i < w_pre; ++i) {
+            mbar_arrive_expect_tx(&fullW[i], kPStageW);
+            tma_load_2d(sW + i * kPStageW, &tmW, &fullW[i], kb * kBlockK, tile * kTileA, pol);
+            if (++kb == p.kb_tile) {
+                kb = 0;
+                ++tile;
+            }
+        }
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (blockIdx.x == 0 && threadIdx.x == 0) *p.epoch_word = p.epoch;
     // let the completion (a programmatic dependent launch) get scheduled early; it waits for
@@ -161,10 +179,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
             int tile = static_cast<int>(x_begin / p.kb_tile);
             int kb = static_cast<int>(x_begin) - tile * p.kb_tile;
             for (uint32_t x = x_begin; x < x_end; ++x) {
-                if (!bwait(&empty[stage], phase ^ 1u, wc)) break;
-                mbar_arrive_expect_tx(&full[stage], bytes);
-                tma_load_2d(ring + stage * bytes, tm, &full[stage], kb * kBlockK,
-                            is_w ? tile * kTileA : 0, pol);
+                if (!(is_w && issued < w_pre)) {  // those were issued before the wait
+                    if (!bwait(&empty[stage], phase ^ 1u, wc)) break;
+                    mbar_arrive_expect_tx(&full[stage], bytes);
+                    tma_load_2d(ring + stage * bytes, tm, &full[stage], kb * kBlockK,
+                                is_w ? tile * kTileA : 0, pol);
+                }
                 ++issued;
                 if (++stage == stages) {
                     stage = 0;

@@ -297,6 +297,10 @@ int32_t sb_merge_shard_payload(const void *payload, int64_t M, int32_t k, int32_
  * second kernel (a programmatic dependent of the first) sums each tile's pieces in
  * ascending K order (lane 0's first), so the result bits do not depend on scheduling.  Two
  * kernels are enqueued on stream; returns SB_OK or an error with nothing enqueued.
+ * The first kernel is a programmatic dependent launch: it starts loading W before the
+ * preceding kernel in the stream has finished, so W must not be written by a kernel that
+ * can still be running then (one that signals its dependents early); X and the workspace
+ * are read only after that kernel has finished.
  * sb_partial_workspace_bytes depends on the shape and on the SM count of the current
  * device; it returns 0 for an invalid shape or when no CUDA device is usable.
  */
