@@ -162,9 +162,13 @@ __global__ void __launch_bounds__(32 * kMaxWarps) combine_kernel(const CombinePa
         if (GUMBEL) gacc = gmerge(gacc, GRec{sgk[s2], sgi[s2], sgz[s2]});
     }
     const float lse = acc.m + logf(acc.s);
-    p.token[row] = GUMBEL ? gacc.i : acc.i;
+    const int tok = GUMBEL ? gacc.i : acc.i;
+    const float tlp = GUMBEL ? gacc.z * p.inv_t - lse : -logf(acc.s);
+    p.token[row] = tok;
     if (p.lse) p.lse[row] = lse;
-    if (p.token_logprob) p.token_logprob[row] = GUMBEL ? gacc.z * p.inv_t - lse : -logf(acc.s);
+    if (p.token_logprob) p.token_logprob[row] = tlp;
+    if (p.token_host) p.token_host[row] = tok;
+    if (p.token_logprob_host) p.token_logprob_host[row] = tlp;
     if (p.target_logprob) {
         const float tz = p.ws.tz[row];
         p.target_logprob[row] = (GUMBEL ? tz * p.inv_t : tz) - lse;
@@ -433,6 +437,8 @@ __global__ void __launch_bounds__(32 * kMaxWarps) combine_topk_kernel(const Comb
     p.token[row] = acc.i;
     if (p.lse) p.lse[row] = lse;
     if (p.token_logprob) p.token_logprob[row] = -logf(acc.s);
+    if (p.token_host) p.token_host[row] = acc.i;
+    if (p.token_logprob_host) p.token_logprob_host[row] = -logf(acc.s);
     if (p.target_logprob) p.target_logprob[row] = p.ws.tz[row] - lse;
 }
 
@@ -505,6 +511,45 @@ cudaError_t launch_merge_payload(const CombineParams &c, const void *payload,
     const unsigned char *pl = static_cast<const unsigned char *>(payload);
     if (c.flags & kFlagGumbel) return cudaLaunchKernelEx(&cfg, merge_payload_kernel<true>, c, pl);
     return cudaLaunchKernelEx(&cfg, merge_payload_kernel<false>, c, pl);
+}
+
+}  // namespace sb
+
+namespace sb {
+namespace {
+
+// Host-to-device copy by the SMs: src is host memory the device can address (pinned and
+// mapped), read in 16-byte words.  Triggers its dependents at entry (the GEMM's setup
+// overlaps the copy) and writes dst only after the previous kernel in the stream has ended
+// (that kernel may still be reading dst).
+__global__ void copy16_kernel(uint4 *dst, const uint4 *src, size_t n16) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+         i += stride)
+        dst[i] = src[i];
+}
+
+}  // namespace
+
+cudaError_t launch_copy16(void *dst, const void *src, size_t n16, int num_sms,
+                          cudaStream_t stream) {
+    if (n16 == 0) return cudaSuccess;
+    constexpr int kThreadsCopy = 256;
+    size_t blocks = (n16 + kThreadsCopy - 1) / kThreadsCopy;
+    if (blocks > static_cast<size_t>(num_sms) * 4) blocks = static_cast<size_t>(num_sms) * 4;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kThreadsCopy);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, copy16_kernel, static_cast<uint4 *>(dst),
+                              static_cast<const uint4 *>(src), n16);
 }
 
 }  // namespace sb

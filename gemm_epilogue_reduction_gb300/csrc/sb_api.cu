@@ -273,6 +273,19 @@ int32_t sb_tiles_per_shard(int64_t M, int64_t V, int32_t k) {
 
 namespace {
 
+// The device address of host memory the device can read and write directly (pinned and
+// mapped, as cudaHostAlloc / cudaHostRegister memory is under unified addressing); null
+// for any other memory (pageable host memory, device memory, unknown pointers).
+void *device_view(const void *host) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+        cudaGetLastError();  // an unknown pointer leaves an error behind: clear it
+        return nullptr;
+    }
+    if (a.type != cudaMemoryTypeHost || !a.devicePointer) return nullptr;
+    return a.devicePointer;
+}
+
 // A validated call: kernel parameters and tensor maps, ready to enqueue.
 struct Prepared {
     GemmParams p;
@@ -395,10 +408,29 @@ int32_t sb_lmhead_project_from_host(const void *H_host, void *H_dev, const void 
     if (int32_t e = prepare(H_dev, W, M, d, V, k, surface, temperature, seed, out, &pr)) return e;
     if (token_logprob_host && !out->token_logprob) return SB_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (cudaMemcpyAsync(H_dev, H_host, static_cast<size_t>(M) * d * 2, cudaMemcpyHostToDevice,
-                        st) != cudaSuccess)
+    const size_t h_bytes = static_cast<size_t>(M) * d * 2;  // a multiple of 16 (d % 8 == 0)
+    // Host buffers the device can address (pinned and mapped) are read and written by the
+    // kernels themselves: no copy-engine operations, whose fixed cost is several
+    // microseconds each.  Other host memory goes through cudaMemcpyAsync.
+    const void *h_view = device_view(H_host);
+    int32_t *tok_view = static_cast<int32_t *>(device_view(token_host));
+    float *lp_view = token_logprob_host ? static_cast<float *>(device_view(token_logprob_host))
+                                        : nullptr;
+    const bool results_direct = tok_view && aligned(tok_view, 4) &&
+                                (!token_logprob_host || (lp_view && aligned(lp_view, 4)));
+    if (h_view && aligned(h_view, 16)) {
+        if (launch_copy16(H_dev, h_view, h_bytes / 16, pr.sms, st) != cudaSuccess)
+            return SB_ERR_CUDA;
+    } else if (cudaMemcpyAsync(H_dev, H_host, h_bytes, cudaMemcpyHostToDevice, st) !=
+               cudaSuccess) {
         return SB_ERR_CUDA;
+    }
+    if (results_direct) {
+        pr.c.token_host = tok_view;
+        pr.c.token_logprob_host = lp_view;
+    }
     if (int32_t e = launch(pr, stream, true)) return e;
+    if (results_direct) return SB_OK;
     // token and log-prob stored back to back on both sides: one copy
     const size_t n = static_cast<size_t>(M) * 4;
     const bool joined =

@@ -92,6 +92,10 @@ struct CombineParams {
     float *token_logprob;
     float *lse;
     float *target_logprob;
+    // optional second copies of token / token_logprob in host memory the device can address
+    // (pinned, mapped): the host-buffer entry point's results, written without a copy
+    int32_t *token_host;
+    float *token_logprob_host;
 };
 
 // Launchers (lmhead.cu, combine.cu).  Return cudaSuccess or the launch error.
@@ -102,6 +106,10 @@ cudaError_t launch_pack(const Workspace &ws, int M, int k, int T, bool gumbel,
                         long long col_offset, void *payload, cudaStream_t stream);
 cudaError_t launch_merge_payload(const CombineParams &c, const void *payload,
                                  cudaStream_t stream);
+// Copies n16 16-byte words from src (host memory the device can address) to dst (device),
+// as a programmatic dependent launch that writes dst only after the previous kernel ends.
+cudaError_t launch_copy16(void *dst, const void *src, size_t n16, int num_sms,
+                          cudaStream_t stream);
 
 size_t lmhead_smem_bytes(int nb, int stages_a, int stages_b, bool vocab_mode, int flags,
                          int topk);

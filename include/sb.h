@@ -176,19 +176,25 @@ int32_t sb_lmhead_records(const void *H, const void *W, int64_t M, int64_t d, in
 /*
  * sb_lmhead_project for a caller whose hidden states are in host memory and who wants the
  * token surface back in host memory ("SemBridge", Section 5.2: the consumer observes the
- * projected surface, never the logits).  Enqueues on stream, in order: one copy of H_host
- * into H_dev, the projection of sb_lmhead_project on H_dev, and one copy each of out->token
- * into token_host and (when token_logprob_host is not NULL) of out->token_logprob into
- * token_logprob_host.
- *   H_host              host bf16 [M, d]; pinned memory makes the copy asynchronous.
- *   H_dev               device staging buffer of M * d bf16, 16-byte aligned; overwritten.
+ * projected surface, never the logits).  Enqueues on stream, in order: H_host into H_dev,
+ * the projection of sb_lmhead_project on H_dev, and the token (and, when
+ * token_logprob_host is not NULL, the chosen log-probability) into the host buffers; the
+ * device outputs in out are written as well.
+ * Host buffers the device can address (pinned memory from cudaHostAlloc or
+ * cudaHostRegister, mapped under unified addressing) are moved by the kernels themselves:
+ * a copy kernel reads H_host and the combine writes the host results directly, with no
+ * copy-engine operations.  Other host memory (pageable) is moved with cudaMemcpyAsync
+ * (synchronous with respect to the host for pageable memory).
+ *   H_host              host bf16 [M, d].
+ *   H_dev               device staging buffer of M * d bf16, 16-byte aligned; overwritten
+ *                       once the previous kernel in the stream has finished.
  *   out                 device outputs and workspace as for sb_lmhead_project.
  *   token_host          host int32 [M] (required); token_logprob_host host float [M] or NULL
- *                       (then out->token_logprob may be NULL); pinned for asynchronous copies.
- * When out->token_logprob directly follows out->token (M int32) and token_logprob_host
- * directly follows token_host, both come back in one copy.  The caller synchronises stream
- * before reading the host outputs.  Every argument is checked before anything is enqueued;
- * returns an sb_status.
+ *                       (then out->token_logprob may be NULL).
+ * On the copy path, when out->token_logprob directly follows out->token (M int32) and
+ * token_logprob_host directly follows token_host, both come back in one copy.  The caller
+ * synchronises stream before reading the host outputs.  Every argument is checked before
+ * anything is enqueued; returns an sb_status.
  */
 int32_t sb_lmhead_project_from_host(const void *H_host, void *H_dev, const void *W, int64_t M,
                                     int64_t d, int64_t V, int32_t k, int32_t surface,

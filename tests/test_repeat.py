@@ -23,12 +23,16 @@ def _built():
     (16, 1024, 151936, 4, sb.SB_TOKEN_LOGPROB, 300),   # vocab mode, decode shape
     (64, 512, 65536, 2, sb.SB_FULL_LOGITS, 200),       # vocab mode, full logits
     (4096, 6144, 200064, 4, sb.SB_TOKEN_LOGPROB, 20),  # the prefill shape, 16 M pairs
+    (16, 1024, 151936, 4, sb.SB_TOPK_LOGPROB, 300),    # vocab mode, top-8 lists
+    (300, 512, 32768, 2, sb.SB_TOPK_LOGPROB, 100),     # rows mode, top-8 lists
 ])
 def test_many_calls_give_identical_bits(M, d, V, k, surface, calls):
     H, W = synth.make_hw(M, d, V, seed=M + d, device="cuda")
-    out, bufs = sb.make_outputs(M, V, k, surface)
+    topk = 8 if surface == sb.SB_TOPK_LOGPROB else 0
+    out, bufs = sb.make_outputs(M, V, k, surface, topk=topk)
     T = 0.8 if surface == sb.SB_GUMBEL_TOKEN else 1.0
     keys = ["token", "token_logprob", "lse"] + (["logits"] if surface == sb.SB_FULL_LOGITS else [])
+    keys += ["topk_ids", "topk_logprob"] if topk else []
 
     def call():
         assert sb.sb_lmhead_project(H, W, M, d, V, k, surface, T, 99, out) == sb.SB_OK
