@@ -14,9 +14,10 @@
 //   warps 0, 2  one lane each issues TMA loads of 64-wide K slices of one operand into its
 //               own ring of shared-memory stages (128-byte swizzle); the ring of the
 //               operand streamed from HBM (W) is deeper than the one re-read from L2 (H);
-//   warp 1      owns the TMEM allocation; one lane issues tcgen05.mma (M = 128,
-//               bf16 x bf16 -> fp32) into one of two TMEM accumulators and commits
-//               stage releases and "accumulator full" to mbarriers;
+//   warp 1      owns the TMEM allocation; one lane issues tcgen05.mma (M = 128, or
+//               M = 256 over a CTA pair in rows mode; bf16 x bf16 -> fp32) into one of two
+//               TMEM accumulators and commits stage releases and "accumulator full" to
+//               mbarriers;
 //   warps 3-10  the epilogue, two warps per TMEM lane quadrant: tcgen05.ld of the finished
 //               accumulator (warp w reads TMEM lanes 32*(w%4) .. +31), mask columns outside
 //               the tile's shard, fold the projection records, release the accumulator.
@@ -25,8 +26,8 @@
 //               M rows of H (UMMA N = M rounded up to 16).  TMEM lane = vocabulary
 //               column; the epilogue reduces across lanes with warp reductions.
 //   rows mode  (M > 128, sampling batches and prefill scoring): A = 128 rows of H, B = 256
-//               rows of W.  TMEM lane = row of H; each epilogue thread folds half of its
-//               row's 256 columns serially.
+//               rows of W (half of them staged by each CTA of a pair).  TMEM lane = row of
+//               H; each epilogue thread folds half of its row's 256 columns serially.
 // Every record covers 128 vocabulary columns (one vocab-mode tile, half a rows-mode tile).
 // Vocabulary tiles never cross a lane-shard boundary: tile t of shard s starts at
 // s*S + t*TV and is masked at (s+1)*S, so each record belongs to one shard.
