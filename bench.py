@@ -95,8 +95,8 @@ NOMINAL_PEAKS = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0}
 # null once the source differs.
 KERNEL_TRAFFIC = {
     # decode16: dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
-    # (1,556,263,168 + 3,237,888 B; W + H are 1,555,988,480 B).
-    "decode16": {"bytes": 1559501056, "src_sha": "4b7fd1e55bcd873b"},
+    # (1,556,124,928 + 3,206,400 B; W + H are 1,555,988,480 B).
+    "decode16": {"bytes": 1559331328, "src_sha": "c7a8ed763ec08d7e"},
 }
 
 
