@@ -1,6 +1,6 @@
 """sb_lmhead_project_from_host: the projection with host-memory hidden states and host-memory
-token outputs gives exactly the bits of sb_lmhead_project on the same inputs, for pinned and
-for pageable host buffers."""
+token outputs gives exactly the bits of sb_lmhead_project on the same inputs, for pinned
+buffers (moved by the kernels), pageable buffers (copied), and mixtures of the two."""
 import pytest
 import torch
 
@@ -62,3 +62,35 @@ def test_host_buffer_call_with_token_and_logprob_back_to_back():
     torch.cuda.synchronize()
     assert torch.equal(res_host[:M], ref["token"].cpu())
     assert torch.equal(res_host[M:].view(torch.float32), ref["token_logprob"].cpu())
+
+
+@pytest.mark.parametrize("case", ["H_unaligned", "logprob_pageable", "token_pageable"])
+def test_host_buffer_call_with_mixed_buffers(case):
+    """A pinned H at an address that is not 16-byte aligned is copied; pinned and pageable
+    result buffers mixed in one call are copied: the bits stay those of the device call."""
+    M, d, V, k = 16, 512, 40000, 4
+    H, W = synth.make_hw(M, d, V, seed=21, device="cuda")
+    ref = sb.project(H, W, k, sb.SB_TOKEN_LOGPROB)
+    n = M * d
+    if case == "H_unaligned":
+        back = torch.empty(n + 4, dtype=torch.bfloat16).pin_memory()
+        H_host = back[4:]  # 8 bytes past a 16-byte boundary
+        H_host.copy_(H.cpu().reshape(-1))
+        assert H_host.data_ptr() % 16 == 8
+    else:
+        H_host = H.cpu().pin_memory()
+    tok_host = torch.full((M,), -1, dtype=torch.int32)
+    lp_host = torch.full((M,), float("nan"), dtype=torch.float32)
+    if case != "token_pageable":
+        tok_host = tok_host.pin_memory()
+    if case != "logprob_pageable":
+        lp_host = lp_host.pin_memory()
+    H_dev = torch.empty_like(H)
+    out, bufs = sb.make_outputs(M, V, k, sb.SB_TOKEN_LOGPROB)
+    st = sb.sb_lmhead_project_from_host(H_host, H_dev, W, M, d, V, k, sb.SB_TOKEN_LOGPROB, 1.0,
+                                        0, out, tok_host, lp_host)
+    assert st == sb.SB_OK
+    torch.cuda.synchronize()
+    assert torch.equal(H_dev, H)
+    assert torch.equal(tok_host, ref["token"].cpu())
+    assert torch.equal(lp_host, ref["token_logprob"].cpu())
