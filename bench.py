@@ -57,6 +57,8 @@ WORKLOADS = {
                  desc="tiny: H[4,256] x W[4096,256] bf16, k=2"),
     "decode16_topk": dict(M=16, d=5120, V=151936, k=4, surface="topk_logprob", topk=8,
                           desc="decode top-8 log-probs: H[16,5120] x W[151936,5120] bf16, k=4"),
+    "sampling_topk": dict(M=256, d=5120, V=151936, k=4, surface="topk_logprob", topk=8,
+                          desc="256-row batch, top-8 log-probs: H[256,5120] x W[151936,5120] bf16, k=4"),
     "sampling_token": dict(M=256, d=5120, V=151936, k=4, surface="token_logprob",
                            desc="256-row decode batch: H[256,5120] x W[151936,5120] bf16, k=4, TOKEN + log-prob"),
     "mlp_down": dict(kind="partial", M=64, N=5120, K=17408, lanes=2,

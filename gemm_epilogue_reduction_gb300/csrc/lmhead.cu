@@ -439,7 +439,8 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
                                               int lane, uint32_t tempty_remote) {
     constexpr bool GUMBEL = EPI == kEpiGumbel;
     constexpr bool FULL = EPI == kEpiFull;
-    constexpr bool TOPK = EPI == kEpiTopk;
+    constexpr bool TOPK = EPI == kEpiTopk || EPI == kEpiTopk8 || EPI == kEpiTopk4;
+    constexpr int KL = EPI == kEpiTopk4 ? 4 : (EPI == kEpiTopk8 ? 8 : kMaxTopK);
     const int row = c.m0 + 32 * q + lane;
     const bool rv = row < p.M;
     const int rt = 2 * c.t + h;                 // record tile within the shard
@@ -447,13 +448,13 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
     const int tgt = ((p.flags & kFlagTargets) && rv) ? __ldg(p.targets + row) : -1;
     float rm = -INFINITY, rs = 0.f, gk = -INFINITY, gz = 0.f;
     int ri = INT_MAX, gi = INT_MAX;
-    // top-K: a sorted list (largest first, equal values by ascending column) of the
-    // kMaxTopK largest seen; only the first K are written
-    float tv[TOPK ? kMaxTopK : 1];
-    int ti[TOPK ? kMaxTopK : 1];
+    // top-K: a sorted list (largest first, equal values by ascending column) of the KL
+    // largest seen (KL >= K); only the first K are written
+    float tv[TOPK ? KL : 1];
+    int ti[TOPK ? KL : 1];
     if (TOPK) {
 #pragma unroll
-        for (int r = 0; r < kMaxTopK; ++r) {
+        for (int r = 0; r < KL; ++r) {
             tv[r] = -INFINITY;
             ti[r] = INT_MAX;
         }
@@ -514,28 +515,24 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
             }
         }
         if (TOPK) {
+            // insertion without branches: entry r becomes the old entry r-1 if y beats it,
+            // else y if y beats entry r, else stays; a y that beats no entry changes nothing
+            // (invalid columns are -inf).  Columns arrive in ascending order, so an equal
+            // value already in the list has a lower column and stays ahead.
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                if (y[j] > tv[kMaxTopK - 1]) {  // invalid columns are -inf: never inserted
-                    // columns arrive in ascending order, so an equal value already in the
-                    // list has a lower column and stays ahead; after the insertion point
-                    // every entry shifts down by one
-                    float cv = y[j];
-                    int ci = cb + j;
-                    bool ins = false;
+                const float x = y[j];
+                const int xc = cb + j;
+                bool gt[KL];
 #pragma unroll
-                    for (int r = 0; r < kMaxTopK; ++r) {
-                        if (ins || cv > tv[r]) {
-                            const float tvr = tv[r];
-                            const int tir = ti[r];
-                            tv[r] = cv;
-                            ti[r] = ci;
-                            cv = tvr;
-                            ci = tir;
-                            ins = true;
-                        }
-                    }
+                for (int r = 0; r < KL; ++r) gt[r] = x > tv[r];
+#pragma unroll
+                for (int r = KL - 1; r >= 1; --r) {
+                    tv[r] = gt[r - 1] ? tv[r - 1] : (gt[r] ? x : tv[r]);
+                    ti[r] = gt[r - 1] ? ti[r - 1] : (gt[r] ? xc : ti[r]);
                 }
+                tv[0] = gt[0] ? x : tv[0];
+                ti[0] = gt[0] ? xc : ti[0];
             }
         }
         if (tgt >= cb && tgt < cb + nval) {
@@ -579,7 +576,7 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
         }
         if (TOPK) {
 #pragma unroll
-            for (int r = 0; r < kMaxTopK; ++r) {
+            for (int r = 0; r < KL; ++r) {
                 if (r >= p.topk) break;
                 p.ws.tkv[o * p.topk + r] = tv[r];
                 p.ws.tki[o * p.topk + r] = ti[r];
@@ -1001,8 +998,10 @@ cudaError_t launch_lmhead(bool vocab_mode, const CUtensorMap &tmA, const CUtenso
         return vocab_mode ? launch_t<true, kEpiFull, 1>(tmA, tmB, p, smem, num_sms, stream)
                           : launch_t<false, kEpiFull, C>(tmA, tmB, p, smem, num_sms, stream);
     case kEpiTopk:
-        return vocab_mode ? launch_t<true, kEpiTopk, 1>(tmA, tmB, p, smem, num_sms, stream)
-                          : launch_t<false, kEpiTopk, C>(tmA, tmB, p, smem, num_sms, stream);
+        if (vocab_mode) return launch_t<true, kEpiTopk, 1>(tmA, tmB, p, smem, num_sms, stream);
+        if (p.topk <= 4) return launch_t<false, kEpiTopk4, C>(tmA, tmB, p, smem, num_sms, stream);
+        if (p.topk <= 8) return launch_t<false, kEpiTopk8, C>(tmA, tmB, p, smem, num_sms, stream);
+        return launch_t<false, kEpiTopk, C>(tmA, tmB, p, smem, num_sms, stream);
     default:
         return vocab_mode ? launch_t<true, kEpiPlain, 1>(tmA, tmB, p, smem, num_sms, stream)
                           : launch_t<false, kEpiPlain, C>(tmA, tmB, p, smem, num_sms, stream);

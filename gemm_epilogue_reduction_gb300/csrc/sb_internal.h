@@ -40,7 +40,10 @@ constexpr int kMaxTopKShards = 128;  // largest k with the top-K surface (combin
 // Surface flags the kernels specialise on.
 enum : int { kFlagGumbel = 1, kFlagFull = 2, kFlagTargets = 4, kFlagTopk = 8 };
 // Epilogue variants (one per surface family).
-enum : int { kEpiPlain = 0, kEpiFull = 1, kEpiGumbel = 2, kEpiTopk = 3 };
+// The top-K family has one variant per list length (rows mode keeps a sorted list of the
+// smallest of 4, 8, 16 entries that holds K per thread; vocab mode uses kEpiTopk for any K).
+enum : int { kEpiPlain = 0, kEpiFull = 1, kEpiGumbel = 2, kEpiTopk = 3, kEpiTopk8 = 4,
+             kEpiTopk4 = 5 };
 
 struct Workspace {       // device views into the caller's workspace
     uint32_t *epoch;     // header word 0
