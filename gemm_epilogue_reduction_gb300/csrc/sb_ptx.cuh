@@ -60,16 +60,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, ui
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "l"(policy)
         : "memory");
 }
-// Untiled bulk copy global -> shared of `bytes` (a multiple of 16, both addresses 16-byte
-// aligned), completion counted on `bar` in bytes.
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
-                                          uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes),
-        "r"(smem_u32(bar))
-        : "memory");
-}
 // CTA-pair variant: the box lands in this CTA's shared memory and completes its bytes on
 // the mbarrier at cluster address `bar_cluster` (the pair leader's barrier).
 __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *tm,
