@@ -84,3 +84,29 @@ def test_partial_completion_replays_from_a_cuda_graph():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(again, Y)
+
+
+def test_host_buffer_decode_step_replays_from_a_cuda_graph():
+    """The host-buffer call captured once: each replay reads the current contents of the
+    pinned H buffer and leaves the token and log-prob in the pinned result buffers (the
+    copy kernel and the combine's host stores are ordinary graph kernel nodes)."""
+    M, d, V, k = 16, 512, 40000, 4
+    H, W = synth.make_hw(M, d, V, seed=12, device="cuda")
+    H_host = H.cpu().pin_memory()
+    H_dev = torch.empty_like(H)
+    tok = torch.full((M,), -1, dtype=torch.int32).pin_memory()
+    lp = torch.full((M,), float("nan"), dtype=torch.float32).pin_memory()
+    out, bufs = sb.make_outputs(M, V, k, sb.SB_TOKEN_LOGPROB)
+    g = _capture(lambda s: sb.sb_lmhead_project_from_host(H_host, H_dev, W, M, d, V, k,
+                                                          sb.SB_TOKEN_LOGPROB, 1.0, 0, out,
+                                                          tok, lp, s))
+    for trial in range(3):
+        Hn, _ = synth.make_hw(M, d, 1, seed=300 + trial)
+        H_host.copy_(Hn)             # new inputs in the captured host buffer
+        tok.fill_(-1)
+        g.replay()
+        torch.cuda.synchronize()
+        ref = sb.project(Hn.cuda(), W, k, sb.SB_TOKEN_LOGPROB)
+        torch.cuda.synchronize()
+        assert torch.equal(tok, ref["token"].cpu())
+        assert torch.equal(lp, ref["token_logprob"].cpu())
