@@ -109,6 +109,17 @@ def test_topk_decode_shape():
     check_topk(res, H, W, K)
 
 
+def test_topk_sampling_batch_shape():
+    """The 256-row batch shape (rows mode, CTA pairs, 8-entry lists) with K = 8; rows from
+    both M tiles of the pair, checked against the oracle."""
+    M, d, V, k, K = 256, 5120, 151936, 4, 8
+    H, W = synth.make_hw(M, d, V, seed=0, device="cuda")
+    res = sb.project(H, W, k, sb.SB_TOPK_LOGPROB, topk=K)
+    torch.cuda.synchronize()
+    assert sb.sb_last_device_status(res["_outputs"]) == sb.SB_OK
+    check_topk(res, H, W, K, rows=[0, 77, 128, 255])
+
+
 @pytest.mark.parametrize("M,d,V,k", [(16, 256, 4096, 4), (300, 64, 2000, 2)])
 def test_topk_surface_token_and_lse_bits_equal_the_token_surface(M, d, V, k):
     """The top-K combine completes lse and the token with the same fixed tree as the token
