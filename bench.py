@@ -82,6 +82,8 @@ WORKLOADS = {
                            desc="profiling case: H[64,1024] x W[151936,1024] bf16, k=2, FULL_LOGITS"),
     "decode64_token_small": dict(M=64, d=1024, V=151936, k=2, surface="token_logprob",
                                  desc="profiling case: H[64,1024] x W[151936,1024] bf16, k=2, TOKEN_LOGPROB"),
+    "sampling_topk_small": dict(M=256, d=1024, V=151936, k=4, surface="topk_logprob", topk=8,
+                                desc="profiling case: H[256,1024] x W[151936,1024] bf16, k=4, top-8"),
     "sampling_small": dict(M=256, d=1024, V=151936, k=4, surface="gumbel_token", T=0.7,
                            seed=1234,
                            desc="profiling case: H[256,1024] x W[151936,1024] bf16, k=4, GUMBEL"),
@@ -97,8 +99,8 @@ NOMINAL_PEAKS = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0}
 # null once the source differs.
 KERNEL_TRAFFIC = {
     # decode16: dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
-    # (1,556,124,928 + 3,206,400 B; W + H are 1,555,988,480 B).
-    "decode16": {"bytes": 1559331328, "src_sha": "c7a8ed763ec08d7e"},
+    # (1,556,126,720 + 2,895,360 B; W + H are 1,555,988,480 B).
+    "decode16": {"bytes": 1559022080, "src_sha": "7af402b8a1f568c1"},
 }
 
 
