@@ -51,6 +51,9 @@ class sb_outputs(ctypes.Structure):
 def lib():
     """The loaded libsb.so; raises if it has not been built."""
     global _lib
+    L = _lib
+    if L is not None:  # the common case: no lock once loaded
+        return L
     with _lock:
         if _lib is not None:
             return _lib
