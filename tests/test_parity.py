@@ -193,6 +193,17 @@ def test_degenerate_and_extreme_shapes(M, d, V, k):
         assert torch.allclose(res["token_logprob"], torch.zeros_like(res["token_logprob"]))
 
 
+@pytest.mark.parametrize("M,surface", [(4, sb.SB_TOKEN_LOGPROB), (300, sb.SB_GUMBEL_TOKEN)])
+def test_million_column_vocabulary(M, surface):
+    """V = 2^20 + 8 (k = 8 shards of 131,073 columns: a ragged last record in every shard),
+    in both tilings; sampled rows for the 300-row case.  Column indices, stream indices
+    r*V + j and record offsets all exceed 2^20."""
+    V, d, k = (1 << 20) + 8, 64, 8
+    rows = None if M == 4 else [0, 131, 299]
+    run_and_check(M, d, V, k, surface, seed=5, T=0.9, gseed=2024, targets=(M == 4),
+                  rows=rows, device_inputs=True)
+
+
 def test_topk_at_its_limits():
     """K = 16 with k = 128 lanes (the top-K limits)."""
     from test_topk import check_topk
