@@ -1,6 +1,7 @@
 /*
  * A plain C caller of libsb: device memory from cudaMalloc, the projection through the C ABI
- * of sb.h, results compared with the fp64 oracle (liboracle) linked into this test program.
+ * of sb.h, results compared with the fp64 oracle (liboracle) linked into this test program;
+ * then the host-buffer call with pinned and with pageable host memory against those results.
  * Built and run by tests/test_c_abi.py on a GPU machine; exits 0 on agreement.
  */
 #include <cuda_runtime_api.h>
@@ -92,6 +93,43 @@ int main(void) {
             CHECK(Z[r * V + tok[r]] >= t1[r] - 1e-2);
         CHECK(fabs(lse[r] - rlse[r]) <= 5e-3);
         CHECK(fabs(lp[r] - (Z[r * V + tok[r]] - rlse[r])) <= 5e-3);
+    }
+    /* the host-buffer call: pinned buffers (moved by the kernels) and pageable ones (copied)
+       give the device call's bits */
+    for (int pinned = 0; pinned < 2; ++pinned) {
+        uint16_t *hH = NULL;
+        int32_t *hTok = NULL;
+        float *hLp = NULL;
+        if (pinned) {
+            CHECK(cudaMallocHost((void **)&hH, M * d * 2) == cudaSuccess);
+            CHECK(cudaMallocHost((void **)&hTok, M * 4) == cudaSuccess);
+            CHECK(cudaMallocHost((void **)&hLp, M * 4) == cudaSuccess);
+        } else {
+            hH = malloc(M * d * 2);
+            hTok = malloc(M * 4);
+            hLp = malloc(M * 4);
+        }
+        memcpy(hH, H, M * d * 2);
+        memset(hTok, 0xFF, M * 4);
+        memset(hLp, 0xFF, M * 4);
+        void *dStage;
+        CHECK(cudaMalloc(&dStage, M * d * 2) == cudaSuccess);
+        st = sb_lmhead_project_from_host(hH, dStage, dW, M, d, V, (int32_t)k, SB_TOKEN_LOGPROB,
+                                         1.0f, 0, &out, hTok, hLp, NULL);
+        CHECK(st == SB_OK);
+        CHECK(cudaDeviceSynchronize() == cudaSuccess);
+        CHECK(memcmp(hTok, tok, M * 4) == 0);
+        CHECK(memcmp(hLp, lp, M * 4) == 0);
+        cudaFree(dStage);
+        if (pinned) {
+            cudaFreeHost(hH);
+            cudaFreeHost(hTok);
+            cudaFreeHost(hLp);
+        } else {
+            free(hH);
+            free(hTok);
+            free(hLp);
+        }
     }
     /* invalid arguments are refused before anything runs */
     CHECK(sb_lmhead_project(dH, dW, M, d, V + 1, (int32_t)k, SB_TOKEN, 1.0f, 0, &out, NULL) ==
