@@ -513,6 +513,22 @@ def main():
     e2e_h2d = M * d * 2
     e2e_d2h = 2 * M * 4
 
+    # ---- the same step as a serving loop would run it: captured once (sb_host_step_*),
+    # one graph launch and one stream wait per step
+    hstep = sb.HostStep(H_host, H_dev, W, M, d, V, k, surface, T, gseed, e2e_out, tok_host,
+                        lp_host)
+    for _ in range(3):
+        hstep(stream)
+        stream.synchronize()
+    e0.record(stream)
+    for _ in range(E):
+        hstep(stream)
+        stream.synchronize()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_graph_ms = e0.elapsed_time(e1) / E
+    hstep.close()
+
     ms_per_step = total_ms / K
     value = job_rows_per_s(world, M, ms_per_step)
     gemm_avg = sum(gemm_ms) / K
@@ -569,6 +585,9 @@ def main():
             "e2e": {"value": M / (e2e_ms * 1e-3) * world, "unit": "rows/s",
                     "h2d_bytes_per_step": e2e_h2d, "d2h_bytes_per_step": e2e_d2h,
                     "ms_per_step": e2e_ms},
+            "e2e_host_step": {"value": M / (e2e_graph_ms * 1e-3) * world, "unit": "rows/s",
+                              "ms_per_step": e2e_graph_ms,
+                              "api": "sb_host_step_create once, sb_host_step_launch per step"},
             "clocks": clocks.summary(),
             "gpu_launches": 2 * K,
             "wall_s_timed": t_wall,

@@ -78,6 +78,14 @@ def lib():
                                                   ctypes.c_float, u64,
                                                   ctypes.POINTER(sb_outputs), P, P, P]
         L.sb_lmhead_project_from_host.restype = i32
+        L.sb_host_step_create.argtypes = [P, P, P, i64, i64, i64, i32, i32, ctypes.c_float,
+                                          u64, ctypes.POINTER(sb_outputs), P, P,
+                                          ctypes.POINTER(P)]
+        L.sb_host_step_create.restype = i32
+        L.sb_host_step_launch.argtypes = [P, P]
+        L.sb_host_step_launch.restype = i32
+        L.sb_host_step_destroy.argtypes = [P]
+        L.sb_host_step_destroy.restype = None
         L.sb_combine_shard_records.argtypes = [P, i64, i32, i32, i32, ctypes.c_float,
                                                ctypes.POINTER(sb_outputs), P]
         L.sb_combine_shard_records.restype = i32
@@ -152,6 +160,56 @@ def sb_lmhead_project_from_host(H_host, H_dev, W, M, d, V, k, surface, temperatu
         _ptr(H_host), _ptr(H_dev), _ptr(W), M, d, V, k, surface, float(temperature),
         seed & (2**64 - 1), ctypes.byref(out), _ptr(token_host), _ptr(token_logprob_host),
         _stream(stream)))
+
+
+def sb_host_step_create(H_host, H_dev, W, M, d, V, k, surface, temperature, seed,
+                        out: sb_outputs, token_host, token_logprob_host=None):
+    """Returns (status, handle); the handle is an int (0 on error)."""
+    h = ctypes.c_void_p()
+    st = int(lib().sb_host_step_create(
+        _ptr(H_host), _ptr(H_dev), _ptr(W), M, d, V, k, surface, float(temperature),
+        seed & (2**64 - 1), ctypes.byref(out), _ptr(token_host), _ptr(token_logprob_host),
+        ctypes.byref(h)))
+    return st, (h.value or 0)
+
+
+def sb_host_step_launch(step: int, stream=None) -> int:
+    return int(lib().sb_host_step_launch(step, _stream(stream)))
+
+
+def sb_host_step_destroy(step: int) -> None:
+    lib().sb_host_step_destroy(step)
+
+
+class HostStep:
+    """A host-buffer decode step captured once (sb_host_step_*): call it to enqueue one
+    replay; the buffers passed here are read and written by every replay, so the caller
+    keeps them alive and pinned."""
+
+    def __init__(self, H_host, H_dev, W, M, d, V, k, surface, temperature, seed,
+                 out: sb_outputs, token_host, token_logprob_host=None):
+        self._keep = (H_host, H_dev, W, out, token_host, token_logprob_host)
+        st, self.handle = sb_host_step_create(H_host, H_dev, W, M, d, V, k, surface,
+                                              temperature, seed, out, token_host,
+                                              token_logprob_host)
+        if st != SB_OK:
+            raise SbError(st, "sb_host_step_create")
+
+    def __call__(self, stream=None) -> None:
+        st = sb_host_step_launch(self.handle, stream)
+        if st != SB_OK:
+            raise SbError(st, "sb_host_step_launch")
+
+    def close(self) -> None:
+        if self.handle:
+            sb_host_step_destroy(self.handle)
+            self.handle = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def sb_lmhead_records(H, W, M, d, V, k, surface, temperature, seed, out: sb_outputs,

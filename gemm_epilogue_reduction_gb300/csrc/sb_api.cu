@@ -449,6 +449,70 @@ int32_t sb_lmhead_project_from_host(const void *H_host, void *H_dev, const void 
     return SB_OK;
 }
 
+// A host-buffer decode step captured once into a CUDA graph: the copy kernel, the GEMM and
+// the combine with the host stores, replayed by one graph launch per step.
+struct sb_host_step {
+    cudaGraph_t graph;
+    cudaGraphExec_t exec;
+};
+
+int32_t sb_host_step_create(const void *H_host, void *H_dev, const void *W, int64_t M,
+                            int64_t d, int64_t V, int32_t k, int32_t surface,
+                            float temperature, uint64_t seed, const sb_outputs *out,
+                            int32_t *token_host, float *token_logprob_host,
+                            sb_host_step **step) {
+    if (!step) return SB_ERR_INVALID_ARG;
+    *step = nullptr;
+    if (!H_host || !token_host) return SB_ERR_INVALID_ARG;
+    Prepared pr;
+    if (int32_t e = prepare(H_dev, W, M, d, V, k, surface, temperature, seed, out, &pr)) return e;
+    if (token_logprob_host && !out->token_logprob) return SB_ERR_INVALID_ARG;
+    const void *h_view = device_view(H_host);
+    int32_t *tok_view = static_cast<int32_t *>(device_view(token_host));
+    float *lp_view = token_logprob_host ? static_cast<float *>(device_view(token_logprob_host))
+                                        : nullptr;
+    // only device-addressable host buffers: a graph replays kernels, not pageable copies
+    if (!h_view || !aligned(h_view, 16) || !tok_view || !aligned(tok_view, 4) ||
+        (token_logprob_host && (!lp_view || !aligned(lp_view, 4))))
+        return SB_ERR_UNSUPPORTED;
+    pr.c.token_host = tok_view;
+    pr.c.token_logprob_host = lp_view;
+    cudaStream_t cs = nullptr;
+    if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return SB_ERR_CUDA;
+    cudaGraph_t graph = nullptr;
+    bool ok = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
+    if (ok) {
+        const size_t h_bytes = static_cast<size_t>(M) * d * 2;
+        const bool enq = launch_copy16(H_dev, h_view, h_bytes / 16, pr.sms, cs) == cudaSuccess &&
+                         launch(pr, cs, true) == SB_OK;
+        ok = cudaStreamEndCapture(cs, &graph) == cudaSuccess && enq && graph;
+    }
+    cudaStreamDestroy(cs);
+    cudaGraphExec_t exec = nullptr;
+    if (ok) ok = cudaGraphInstantiate(&exec, graph, 0) == cudaSuccess;
+    if (!ok) {
+        if (graph) cudaGraphDestroy(graph);
+        cudaGetLastError();
+        return SB_ERR_CUDA;
+    }
+    *step = new sb_host_step{graph, exec};
+    return SB_OK;
+}
+
+int32_t sb_host_step_launch(sb_host_step *step, void *stream) {
+    if (!step) return SB_ERR_INVALID_ARG;
+    return cudaGraphLaunch(step->exec, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SB_OK
+               : SB_ERR_CUDA;
+}
+
+void sb_host_step_destroy(sb_host_step *step) {
+    if (!step) return;
+    cudaGraphExecDestroy(step->exec);
+    cudaGraphDestroy(step->graph);
+    delete step;
+}
+
 int32_t sb_combine_shard_records(const void *workspace, int64_t M, int32_t k,
                                  int32_t tiles_per_shard_, int32_t surface, float temperature,
                                  const sb_outputs *out, void *stream) {

@@ -203,6 +203,30 @@ int32_t sb_lmhead_project_from_host(const void *H_host, void *H_dev, const void 
                                     void *stream);
 
 /*
+ * The host-buffer call of a serving loop, captured once: sb_host_step_create checks the
+ * arguments as sb_lmhead_project_from_host does and records that call (the copy kernel
+ * reading H_host, the projection, the combine storing into the host buffers) into a CUDA
+ * graph; sb_host_step_launch enqueues one replay on `stream` (one graph launch, about a
+ * quarter of the host-side time of the plain call); sb_host_step_destroy releases it.
+ * Every buffer is bound at creation: each replay reads the current contents of H_host and
+ * overwrites token_host / token_logprob_host and the device outputs of `out`.
+ *   H_host, token_host, token_logprob_host  host memory the device can address (pinned:
+ *              cudaHostAlloc / cudaHostRegister under unified addressing); other host memory
+ *              gives SB_ERR_UNSUPPORTED (use sb_lmhead_project_from_host).
+ *   step       receives the handle (NULL on any error).
+ * Replays reuse the launch epoch of the creation, so sb_last_device_status reports the worst
+ * device status since then.  Returns an sb_status; creation enqueues nothing on any stream.
+ */
+typedef struct sb_host_step sb_host_step;
+int32_t sb_host_step_create(const void *H_host, void *H_dev, const void *W, int64_t M,
+                            int64_t d, int64_t V, int32_t k, int32_t surface,
+                            float temperature, uint64_t seed, const sb_outputs *out,
+                            int32_t *token_host, float *token_logprob_host,
+                            sb_host_step **step);
+int32_t sb_host_step_launch(sb_host_step *step, void *stream);
+void sb_host_step_destroy(sb_host_step *step);
+
+/*
  * The record combine alone (the second kernel of sb_lmhead_project): reads the per-tile
  * records of `workspace` (layout above; tiles_per_shard = T) and writes token,
  * token_logprob, lse and target_logprob of `out` (those that are non-NULL).  Per row it

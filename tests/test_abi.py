@@ -125,3 +125,17 @@ def test_host_buffer_entry_rejects_missing_host_buffers_before_any_copy():
         st = sb.sb_lmhead_project_from_host(h_host, 0x30000000, 0x40000000, 4, 256, 4096, 2,
                                             sb.SB_TOKEN, 1.0, 0, out, tok_host, None, 0)
         assert st == sb.SB_ERR_INVALID_ARG
+
+
+def test_host_step_rejects_missing_arguments_before_any_capture():
+    out = sb.sb_outputs()
+    lib = sb.lib()
+    h = ctypes.c_void_p(123)
+    assert lib.sb_host_step_create(None, None, None, 16, 512, 40000, 4, sb.SB_TOKEN, 1.0, 0,
+                                   ctypes.byref(out), None, None, ctypes.byref(h)) == \
+        sb.SB_ERR_INVALID_ARG
+    assert h.value is None  # the handle is cleared on every error
+    assert lib.sb_host_step_create(None, None, None, 16, 512, 40000, 4, sb.SB_TOKEN, 1.0, 0,
+                                   ctypes.byref(out), None, None, None) == sb.SB_ERR_INVALID_ARG
+    assert lib.sb_host_step_launch(None, None) == sb.SB_ERR_INVALID_ARG
+    lib.sb_host_step_destroy(None)  # no-op

@@ -94,3 +94,41 @@ def test_host_buffer_call_with_mixed_buffers(case):
     assert torch.equal(H_dev, H)
     assert torch.equal(tok_host, ref["token"].cpu())
     assert torch.equal(lp_host, ref["token_logprob"].cpu())
+
+
+@pytest.mark.parametrize("surface", [sb.SB_TOKEN_LOGPROB, sb.SB_GUMBEL_TOKEN])
+def test_captured_host_step_replays_give_the_device_call_bits(surface):
+    """sb_host_step_*: created once, launched several times with new contents of the pinned
+    H buffer; every launch leaves the device call's token and log-prob in the host buffers."""
+    M, d, V, k = 16, 512, 40000, 4
+    _, W = synth.make_hw(1, d, V, seed=31, device="cuda")
+    H_host = torch.empty(M, d, dtype=torch.bfloat16).pin_memory()
+    H_dev = torch.empty(M, d, dtype=torch.bfloat16, device="cuda")
+    tok = torch.full((M,), -1, dtype=torch.int32).pin_memory()
+    lp = torch.full((M,), float("nan"), dtype=torch.float32).pin_memory()
+    out, bufs = sb.make_outputs(M, V, k, surface)
+    step = sb.HostStep(H_host, H_dev, W, M, d, V, k, surface, 0.8, 17, out, tok, lp)
+    try:
+        for trial in range(4):
+            Hn, _ = synth.make_hw(M, d, 1, seed=500 + trial)
+            H_host.copy_(Hn)
+            tok.fill_(-1)
+            step()
+            torch.cuda.synchronize()
+            ref = sb.project(Hn.cuda(), W, k, surface, temperature=0.8, seed=17)
+            torch.cuda.synchronize()
+            assert torch.equal(tok, ref["token"].cpu()), trial
+            assert torch.equal(lp, ref["token_logprob"].cpu()), trial
+        assert sb.sb_last_device_status(out) == sb.SB_OK
+    finally:
+        step.close()
+
+
+def test_captured_host_step_refuses_pageable_buffers():
+    M, d, V, k = 16, 512, 40000, 4
+    H, W = synth.make_hw(M, d, V, seed=32, device="cuda")
+    out, bufs = sb.make_outputs(M, V, k, sb.SB_TOKEN_LOGPROB)
+    st, h = sb.sb_host_step_create(H.cpu(), torch.empty_like(H), W, M, d, V, k,
+                                   sb.SB_TOKEN_LOGPROB, 1.0, 0, out,
+                                   torch.empty(M, dtype=torch.int32), None)
+    assert st == sb.SB_ERR_UNSUPPORTED and h == 0
