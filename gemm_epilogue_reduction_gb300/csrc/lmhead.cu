@@ -179,6 +179,33 @@ __device__ __forceinline__ void cas_desc(uint32_t &ka, int &ea, uint32_t &kb, in
     ea = e;
 }
 
+// Sums of 8 rows over a warp: a[j] is this lane's term of row j.  Three exchange steps
+// (xor 16, 8, 4) each send half of the rows still held and add the other half's partner
+// terms, so the lane keeps one row, (lane >> 2) & 7; two butterfly steps (xor 2, 1) finish
+// it.  Every lane of a group of four holds the same bits (the adds are commutative).
+__device__ __forceinline__ float transposed_row_sum8(const float (&a)[8], int lane) {
+    const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
+    float b[4], c[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float send = b4 ? a[i] : a[i + 4];
+        const float keep = b4 ? a[i + 4] : a[i];
+        b[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = b3 ? b[i] : b[i + 2];
+        const float keep = b3 ? b[i + 2] : b[i];
+        c[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+    }
+    const float send = b2 ? c[0] : c[1];
+    const float keep = b2 ? c[1] : c[0];
+    float d = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 4);
+    d += __shfl_xor_sync(0xFFFFFFFFu, d, 2);
+    d += __shfl_xor_sync(0xFFFFFFFFu, d, 1);
+    return d;
+}
+
 // ------------------------------------------------------------------ epilogue, vocab mode
 // Thread (warp quadrant q, lane) holds vocabulary column v = v0 + 32q + lane for every row
 // (TMEM columns).  The two warps of a quadrant take alternate 8-row chunks (half h takes
@@ -233,18 +260,18 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
             const float wm = ordered_to_float(om[j]);
             ws[j] = valid ? ex2_approx(fmaf(y[j], kLog2e, -wm * kLog2e)) : 0.f;
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-            for (int j = 0; j < cw; ++j) ws[j] += __shfl_xor_sync(0xFFFFFFFFu, ws[j], off);
-        float my_m = -INFINITY, my_s = 0.f, my_gk = -INFINITY, my_gz = 0.f;
+        // The 8 rows' sums over the 32 lanes in one transposed reduction: each xor step hands
+        // half of the rows a lane still holds to its partner (16: rows 4-7 / 0-3, 8, 4), then
+        // two plain steps; row j ends in lanes 4j .. 4j+3 (identical bits in all four).
+        const int jr = lane >> 2;  // the row this lane ends up holding
+        const float my_s = transposed_row_sum8(ws, lane);
+        float my_m = -INFINITY, my_gk = -INFINITY, my_gz = 0.f;
         int my_i = INT_MAX, my_gi = INT_MAX;
 #pragma unroll
         for (int j = 0; j < cw; ++j)
-            if (lane == j) {
+            if (jr == j) {
                 my_m = ordered_to_float(om[j]);
                 my_i = wi[j];
-                my_s = ws[j];
             }
         if (GUMBEL) {
             // stream index of (row c0 + j, column v) is (c0 + j) V + v: the state advances by
@@ -267,7 +294,7 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
                     __reduce_min_sync(0xFFFFFFFFu, (valid && ok[j] == okm[j]) ? v : INT_MAX);
                 const int src = (gi == INT_MAX) ? 0 : (gi - col0);
                 const float gz = __shfl_sync(0xFFFFFFFFu, __uint_as_float(raw[j]), src & 31);
-                if (lane == j) {
+                if (jr == j) {
                     my_gk = ordered_to_float(okm[j]);
                     my_gi = gi;
                     my_gz = gz;
@@ -283,8 +310,8 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
             if (has_t && tgt_s[row] == v) p.ws.tz[row] = z;
             if (TOPK) zs[row * kVocabTileV + 32 * q + lane] = z;
         }
-        if (lane < cw && c0 + lane < p.M) {
-            const int o = q * nb + c0 + lane;
+        if ((lane & 3) == 0 && c0 + jr < p.M) {
+            const int o = q * nb + c0 + jr;
             sc_m[o] = my_m;
             sc_i[o] = my_i;
             sc_s[o] = my_s;
