@@ -505,17 +505,27 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
         const int nval = min(32, c.v_end - cb);
         if (nval <= 0) continue;
         float y[32];
+        if (nval == 32) {  // a whole chunk (every one but a shard's last): no column mask
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float z = __uint_as_float(raw[j]);
+                y[j] = GUMBEL ? z * p.inv_t : z;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float z = __uint_as_float(raw[j]);
+                y[j] = (j < nval) ? (GUMBEL ? z * p.inv_t : z) : -INFINITY;
+            }
+        }
         float cm = -INFINITY;
         int cj = 0;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const float z = __uint_as_float(raw[j]);
-            y[j] = (j < nval) ? (GUMBEL ? z * p.inv_t : z) : -INFINITY;
+        for (int j = 0; j < 32; ++j)
             if (y[j] > cm) {
                 cm = y[j];
                 cj = j;
             }
-        }
         if (cm > rm) {
             rs *= ex2_approx((rm - cm) * kLog2e);
             rm = cm;
