@@ -633,7 +633,7 @@ __device__ __forceinline__ void produce_ring(const GemmParams &p, const CUtensor
                                              uint64_t policy, int unit0, int unit_stride,
                                              bool vocab, volatile int *abort_flag,
                                              TileCoord (*coord)(const GemmParams &, int, int),
-                                             bool pair) {
+                                             bool pair, uint32_t pre) {
     // pair: the leader's barrier counts both CTAs' bytes; the peer's copies complete on the
     // leader's barrier (at the same offset), and the peer's empty barriers are armed by the
     // leader's MMA commits (cluster-scope acquire)
@@ -646,6 +646,14 @@ __device__ __forceinline__ void produce_ring(const GemmParams &p, const CUtensor
         const TileCoord c = coord(p, tile, rank);
         const int row = is_a ? c.a_row : c.b_row;
         for (int kb = 0; kb < p.kblocks; ++kb) {
+            if (issued < pre) {  // already issued before the wait on the previous kernel
+                ++issued;
+                if (++stage == stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                continue;
+            }
             if (!(pair ? bwait_cl(&empty[stage], phase ^ 1u, abort_flag, p)
                        : bwait(&empty[stage], phase ^ 1u, abort_flag, p))) {
                 ok = false;
@@ -771,8 +779,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     // The setup above touches no global memory, so it overlaps the previous kernel in the
-    // stream (this kernel is a programmatic dependent launch); the inputs and the workspace
-    // may belong to that kernel, so everything from here on waits for it.
+    // stream (this kernel is a programmatic dependent launch).  In vocab mode W (operand A)
+    // is the output-head weight, which that kernel does not write, so ring A's first stages
+    // are filled before the wait (the W stream starts under the previous kernel's tail); H,
+    // the targets and the workspace may belong to that kernel, so everything else waits.
+    uint32_t a_pre = 0;
+    if (VOCAB && warp == 0 && lane == 0 && unit0 < p.num_tiles) {
+        a_pre = static_cast<uint32_t>(p.stages_a < p.kblocks ? p.stages_a : p.kblocks);
+        const TileCoord c = tile_coord<VOCAB, CS>(p, unit0, rank);
+        const uint64_t pol = policy_evict_first();
+        for (uint32_t kb = 0; kb < a_pre; ++kb) {
+            mbar_arrive_expect_tx(&fullA[kb], kStageBytesA);
+            tma_load_2d(sA + kb * kStageBytesA, &tmA, &fullA[kb], static_cast<int>(kb) * kBlockK,
+                        c.a_row, pol);
+        }
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (blockIdx.x == 0 && threadIdx.x == 0) *p.ws.epoch = p.epoch;
     if (VOCAB && (p.flags & kFlagTargets))
@@ -802,13 +823,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          true, false, rank, CS, kClusterMask,
                                          VOCAB ? policy_evict_first() : policy_evict_last(),
                                          unit0, unit_stride, VOCAB, abort_flag,
-                                         coord_fn<VOCAB, CS>, PAIR);
+                                         coord_fn<VOCAB, CS>, PAIR, a_pre);
             else
                 produce_ring<kMaxStages>(p, &tmB, sB, b_stage_bytes, p.stages_b, fullB, emptyB,
                                          false, CS > 1 && !PAIR, rank, CS, kClusterMask,
                                          VOCAB ? policy_evict_last() : policy_evict_normal(),
                                          unit0, unit_stride, VOCAB, abort_flag,
-                                         coord_fn<VOCAB, CS>, PAIR);
+                                         coord_fn<VOCAB, CS>, PAIR, 0u);
         }
     } else if (warp == 1) {
         if (PAIR && rank == 1) {
