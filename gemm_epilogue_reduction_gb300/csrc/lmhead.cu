@@ -794,6 +794,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         c.a_row, pol);
         }
     }
+    // Rows mode with CTA pairs: the same for W, operand B, in both CTAs of the pair (the
+    // peer's copies complete on the leader's barriers, as in the ring loop below).
+    uint32_t b_pre = 0;
+    if (PAIR && warp == 2 && lane == 0 && unit0 < p.num_tiles) {
+        b_pre = static_cast<uint32_t>(p.stages_b < p.kblocks ? p.stages_b : p.kblocks);
+        const TileCoord c = tile_coord<VOCAB, CS>(p, unit0, rank);
+        const uint64_t pol = policy_evict_normal();
+        for (uint32_t kb = 0; kb < b_pre; ++kb) {
+            uint8_t *dst = sB + kb * b_stage_bytes;
+            if (rank == 0) {
+                mbar_arrive_expect_tx(&fullB[kb], 2 * b_stage_bytes);
+                tma_load_2d(dst, &tmB, &fullB[kb], static_cast<int>(kb) * kBlockK, c.b_row, pol);
+            } else {
+                tma_load_2d_pair(dst, &tmB, mapa_rank(&fullB[kb], 0),
+                                 static_cast<int>(kb) * kBlockK, c.b_row, pol);
+            }
+        }
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (blockIdx.x == 0 && threadIdx.x == 0) *p.ws.epoch = p.epoch;
     if (VOCAB && (p.flags & kFlagTargets))
@@ -829,7 +847,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          false, CS > 1 && !PAIR, rank, CS, kClusterMask,
                                          VOCAB ? policy_evict_last() : policy_evict_normal(),
                                          unit0, unit_stride, VOCAB, abort_flag,
-                                         coord_fn<VOCAB, CS>, PAIR, 0u);
+                                         coord_fn<VOCAB, CS>, PAIR, b_pre);
         }
     } else if (warp == 1) {
         if (PAIR && rank == 1) {

@@ -155,10 +155,10 @@ int32_t sb_tiles_per_shard(int64_t M, int64_t V, int32_t k);
  *              g = -log(-log u) in fp32 to within 2e-6 absolute (u = 0 gives g = -inf).
  *              Ignored otherwise.
  *   out        outputs and workspace (see sb_outputs); read on the host during the call.
- * The GEMM is a programmatic dependent launch: for M <= 128 it starts loading W before the
- * preceding kernel in the stream has finished, so W must not be written by a kernel that can
- * still be running then (one that signals its dependents early); H, the targets and the
- * workspace are read only after that kernel has finished.
+ * The GEMM is a programmatic dependent launch that starts loading W before the preceding
+ * kernel in the stream has finished, so W must not be written by a kernel that can still be
+ * running then (one that signals its dependents early); H, the targets and the workspace are
+ * read only after that kernel has finished.
  * Returns SB_OK, or an error with nothing enqueued.
  */
 int32_t sb_lmhead_project(const void *H, const void *W, int64_t M, int64_t d, int64_t V,
