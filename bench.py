@@ -99,8 +99,8 @@ NOMINAL_PEAKS = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0}
 # null once the source differs.
 KERNEL_TRAFFIC = {
     # decode16: dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
-    # (1,556,123,136 + 3,219,968 B; W + H are 1,555,988,480 B).
-    "decode16": {"bytes": 1559343104, "src_sha": "1622f743d0596669"},
+    # (1,556,127,488 + 3,217,152 B; W + H are 1,555,988,480 B).
+    "decode16": {"bytes": 1559344640, "src_sha": "e00d73faa972287d"},
 }
 
 
