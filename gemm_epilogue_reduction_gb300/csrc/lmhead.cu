@@ -65,8 +65,8 @@ __host__ __device__ inline SmemLayout make_layout(int nb, int stages_a, int stag
     L.a_off = off;
     off += stages_a * kStageBytesA;
     L.b_off = off;
-    // rows mode with CTA pairs: each CTA stages only its half of the W tile
-    off += stages_b * ((!vocab && kRowsPair) ? nb / 2 : nb) * 128;
+    // rows mode (CTA pairs): each CTA stages only its half of the W tile
+    off += stages_b * (vocab ? nb : nb / 2) * 128;
     L.bar_off = off;
     off += (4 * kMaxStages + 8) * 8;
     L.misc_off = off;
@@ -88,11 +88,12 @@ struct TileCoord {
 };
 
 // Work unit `tile` of a CTA with cluster rank `rank`.  Vocab mode: one 128-column vocabulary
-// tile.  Rows mode: one 256-column vocabulary tile times a group of CS consecutive M tiles,
-// CTA `rank` of the cluster taking M tile CS*group + rank and loading W rows
-// [v0 + rank*256/CS, +256/CS) of the shared W tile (multicast to the whole cluster).
-template <bool VOCAB, int CS>
+// tile.  Rows mode: one 256-column vocabulary tile times a pair of consecutive M tiles, CTA
+// `rank` of the pair taking M tile 2*group + rank and staging W rows [v0 + 128*rank, +128)
+// of the tile (its half of the pair MMA's B operand).
+template <bool VOCAB>
 __device__ __forceinline__ TileCoord tile_coord(const GemmParams &p, int tile, int rank) {
+    constexpr int CS = VOCAB ? 1 : kRowsCluster;
     TileCoord c;
     const int vt = VOCAB ? tile : tile / p.m_groups;
     const int mt = VOCAB ? 0 : (tile % p.m_groups) * CS + rank;
@@ -629,9 +630,8 @@ template <int NSTAGES_MAX>
 __device__ __forceinline__ void produce_ring(const GemmParams &p, const CUtensorMap *tm,
                                              uint8_t *ring, uint32_t stage_bytes, int stages,
                                              uint64_t *full, uint64_t *empty, bool is_a,
-                                             bool multicast, int rank, int cs, uint16_t mask,
-                                             uint64_t policy, int unit0, int unit_stride,
-                                             bool vocab, volatile int *abort_flag,
+                                             int rank, uint64_t policy, int unit0,
+                                             int unit_stride, volatile int *abort_flag,
                                              TileCoord (*coord)(const GemmParams &, int, int),
                                              bool pair, uint32_t pre) {
     // pair: the leader's barrier counts both CTAs' bytes; the peer's copies complete on the
@@ -663,9 +663,6 @@ __device__ __forceinline__ void produce_ring(const GemmParams &p, const CUtensor
             uint8_t *dst = ring + stage * stage_bytes;
             if (peer)
                 tma_load_2d_pair(dst, tm, mapa_rank(&full[stage], 0), kb * kBlockK, row, policy);
-            else if (multicast)
-                tma_load_2d_mc(dst + rank * (stage_bytes / cs), tm, &full[stage], kb * kBlockK,
-                               row, mask, policy);
             else
                 tma_load_2d(dst, tm, &full[stage], kb * kBlockK, row, policy);
             ++issued;
@@ -676,8 +673,7 @@ __device__ __forceinline__ void produce_ring(const GemmParams &p, const CUtensor
         }
     }
     // Drain: the last `stages` issues may still be landing (only possible after an abort;
-    // on the normal path the MMA warp consumed every one of them).  A stage's barrier also
-    // counts the bytes a cluster peer multicasts into it.
+    // on the normal path the MMA warp consumed every one of them).
     if (peer) {
         // the peer cannot observe its copies (they complete on the leader's barrier); after
         // an abort it gives the last ones a bounded time to land (they were issued at least
@@ -696,12 +692,12 @@ __device__ __forceinline__ void produce_ring(const GemmParams &p, const CUtensor
         if (!bwait_drain(&full[i % stages], (i / stages) & 1u, abort_flag, p)) break;
 }
 
-template <bool VOCAB, int CS>
+template <bool VOCAB>
 __device__ TileCoord coord_fn(const GemmParams &p, int tile, int rank) {
-    return tile_coord<VOCAB, CS>(p, tile, rank);
+    return tile_coord<VOCAB>(p, tile, rank);
 }
 
-template <bool VOCAB, int EPI, int CS>
+template <bool VOCAB, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const GemmParams p, const uint32_t tmem_cols) {
@@ -727,20 +723,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Rows mode with 2-CTA clusters, two schemes (kRowsPair):
-    //  - multicast: each CTA runs its own cta_group::1 MMA on the whole 256-row W tile, of
-    //    which it loads half and receives the other half by TMA multicast from its peer;
-    //  - pair: one cta_group::2 MMA (M = 256) per pair, issued by rank 0, with each CTA
-    //    staging only its half of the W tile (UMMA B split along N) and its own H tile (A
-    //    split along M); each CTA's TMEM holds its 128 rows.  The peer's copies complete on
-    //    the leader's stage barriers, which count both CTAs' bytes.
-    constexpr bool PAIR = !VOCAB && CS == 2 && kRowsPair;
+    // Rows mode runs on CTA pairs (2-CTA clusters): one cta_group::2 MMA (M = 256) per K
+    // step, issued by rank 0, with each CTA staging only its half of the W tile (UMMA B split
+    // along N) and its own H tile (A split along M); each CTA's TMEM holds its 128 rows.  The
+    // peer's copies complete on the leader's stage barriers, which count both CTAs' bytes.
+    constexpr int CS = VOCAB ? 1 : kRowsCluster;
+    constexpr bool PAIR = !VOCAB;
     const uint32_t b_stage_bytes = static_cast<uint32_t>(PAIR ? p.nb / 2 : p.nb) * 128u;
     // CTAs of a cluster walk the same work units in lockstep (same ring positions).
     const int rank = CS > 1 ? static_cast<int>(cluster_ctarank()) : 0;
     const int unit0 = blockIdx.x / CS;
     const int unit_stride = gridDim.x / CS;
-    constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CS) - 1u);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages_a; ++i) {
@@ -749,8 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < p.stages_b; ++i) {
             mbar_init(&fullB[i], 1);
-            // multicast: one MMA commit from every CTA of the cluster; pair: the leader's
-            mbar_init(&emptyB[i], PAIR ? 1 : CS);
+            mbar_init(&emptyB[i], 1);  // one MMA commit (in a pair: the leader's)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
@@ -775,7 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (CS > 1) cluster_sync();  // peers' barriers are initialised before any multicast
+    if (CS > 1) cluster_sync();  // the peer's barriers are initialised before any copy lands
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     // The setup above touches no global memory, so it overlaps the previous kernel in the
@@ -786,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t a_pre = 0;
     if (VOCAB && warp == 0 && lane == 0 && unit0 < p.num_tiles) {
         a_pre = static_cast<uint32_t>(p.stages_a < p.kblocks ? p.stages_a : p.kblocks);
-        const TileCoord c = tile_coord<VOCAB, CS>(p, unit0, rank);
+        const TileCoord c = tile_coord<VOCAB>(p, unit0, rank);
         const uint64_t pol = policy_evict_first();
         for (uint32_t kb = 0; kb < a_pre; ++kb) {
             mbar_arrive_expect_tx(&fullA[kb], kStageBytesA);
@@ -799,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t b_pre = 0;
     if (PAIR && warp == 2 && lane == 0 && unit0 < p.num_tiles) {
         b_pre = static_cast<uint32_t>(p.stages_b < p.kblocks ? p.stages_b : p.kblocks);
-        const TileCoord c = tile_coord<VOCAB, CS>(p, unit0, rank);
+        const TileCoord c = tile_coord<VOCAB>(p, unit0, rank);
         const uint64_t pol = policy_evict_normal();
         for (uint32_t kb = 0; kb < b_pre; ++kb) {
             uint8_t *dst = sB + kb * b_stage_bytes;
@@ -838,16 +830,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             if (warp == 0)
                 produce_ring<kMaxStages>(p, &tmA, sA, kStageBytesA, p.stages_a, fullA, emptyA,
-                                         true, false, rank, CS, kClusterMask,
+                                         true, rank,
                                          VOCAB ? policy_evict_first() : policy_evict_last(),
-                                         unit0, unit_stride, VOCAB, abort_flag,
-                                         coord_fn<VOCAB, CS>, PAIR, a_pre);
+                                         unit0, unit_stride, abort_flag, coord_fn<VOCAB>, PAIR,
+                                         a_pre);
             else
                 produce_ring<kMaxStages>(p, &tmB, sB, b_stage_bytes, p.stages_b, fullB, emptyB,
-                                         false, CS > 1 && !PAIR, rank, CS, kClusterMask,
+                                         false, rank,
                                          VOCAB ? policy_evict_last() : policy_evict_normal(),
-                                         unit0, unit_stride, VOCAB, abort_flag,
-                                         coord_fn<VOCAB, CS>, PAIR, b_pre);
+                                         unit0, unit_stride, abort_flag, coord_fn<VOCAB>, PAIR,
+                                         b_pre);
         }
     } else if (warp == 1) {
         if (PAIR && rank == 1) {
@@ -902,7 +894,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         } else if (lane == 0) {
-            // ------------------------------------------------ MMA issuer (one lane)
+            // ------------------------------------------------ MMA issuer (one lane, vocab mode)
             const uint32_t idesc = idesc_bf16_f32(kTileA, p.nb);
             int sa = 0, sb = 0;
             uint32_t pa = 0, pb = 0;
@@ -928,10 +920,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         umma_bf16(d_tmem, adesc + 2u * ks, bdesc + 2u * ks, idesc,
                                   (kb | ks) != 0 ? 1u : 0u);
                     umma_commit(&emptyA[sa]);
-                    if (CS > 1)
-                        umma_commit_mc(&emptyB[sb], kClusterMask);  // frees it cluster-wide
-                    else
-                        umma_commit(&emptyB[sb]);
+                    umma_commit(&emptyB[sb]);
                     any = true;
                     if (++sa == p.stages_a) {
                         sa = 0;
@@ -966,7 +955,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = bwait(&tfull[b], tph, abort_flag, p);
             if (epi_vote_any(!ok)) break;
             tc_fence_after();
-            const TileCoord c = tile_coord<VOCAB, CS>(p, tile, rank);
+            const TileCoord c = tile_coord<VOCAB>(p, tile, rank);
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * p.nb);
             if (VOCAB)
@@ -992,10 +981,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool VOCAB, int EPI, int CS>
+template <bool VOCAB, int EPI>
 cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p,
                      size_t smem, int num_sms, cudaStream_t stream) {
-    auto kern = lmhead_kernel<VOCAB, EPI, CS>;
+    constexpr int CS = VOCAB ? 1 : kRowsCluster;
+    auto kern = lmhead_kernel<VOCAB, EPI>;
     // The shared-memory opt-in is per device; every launch asks for at most kSmemLimit.
     static std::atomic<uint64_t> opted_in{0};
     int dev = 0;
@@ -1065,22 +1055,21 @@ cudaError_t launch_lmhead(bool vocab_mode, const CUtensorMap &tmA, const CUtenso
                     : (p.flags & kFlagFull) ? kEpiFull
                     : (p.flags & kFlagTopk) ? kEpiTopk
                                             : kEpiPlain;
-    constexpr int C = kRowsCluster;
     switch (epi) {
     case kEpiGumbel:
-        return vocab_mode ? launch_t<true, kEpiGumbel, 1>(tmA, tmB, p, smem, num_sms, stream)
-                          : launch_t<false, kEpiGumbel, C>(tmA, tmB, p, smem, num_sms, stream);
+        return vocab_mode ? launch_t<true, kEpiGumbel>(tmA, tmB, p, smem, num_sms, stream)
+                          : launch_t<false, kEpiGumbel>(tmA, tmB, p, smem, num_sms, stream);
     case kEpiFull:
-        return vocab_mode ? launch_t<true, kEpiFull, 1>(tmA, tmB, p, smem, num_sms, stream)
-                          : launch_t<false, kEpiFull, C>(tmA, tmB, p, smem, num_sms, stream);
+        return vocab_mode ? launch_t<true, kEpiFull>(tmA, tmB, p, smem, num_sms, stream)
+                          : launch_t<false, kEpiFull>(tmA, tmB, p, smem, num_sms, stream);
     case kEpiTopk:
-        if (vocab_mode) return launch_t<true, kEpiTopk, 1>(tmA, tmB, p, smem, num_sms, stream);
-        if (p.topk <= 4) return launch_t<false, kEpiTopk4, C>(tmA, tmB, p, smem, num_sms, stream);
-        if (p.topk <= 8) return launch_t<false, kEpiTopk8, C>(tmA, tmB, p, smem, num_sms, stream);
-        return launch_t<false, kEpiTopk, C>(tmA, tmB, p, smem, num_sms, stream);
+        if (vocab_mode) return launch_t<true, kEpiTopk>(tmA, tmB, p, smem, num_sms, stream);
+        if (p.topk <= 4) return launch_t<false, kEpiTopk4>(tmA, tmB, p, smem, num_sms, stream);
+        if (p.topk <= 8) return launch_t<false, kEpiTopk8>(tmA, tmB, p, smem, num_sms, stream);
+        return launch_t<false, kEpiTopk>(tmA, tmB, p, smem, num_sms, stream);
     default:
-        return vocab_mode ? launch_t<true, kEpiPlain, 1>(tmA, tmB, p, smem, num_sms, stream)
-                          : launch_t<false, kEpiPlain, C>(tmA, tmB, p, smem, num_sms, stream);
+        return vocab_mode ? launch_t<true, kEpiPlain>(tmA, tmB, p, smem, num_sms, stream)
+                          : launch_t<false, kEpiPlain>(tmA, tmB, p, smem, num_sms, stream);
     }
 }
 

@@ -18,16 +18,9 @@ constexpr int kRecordCols = 128;     // vocabulary columns covered by one projec
 constexpr int kMaxVocabModeRows = SB_MAX_VOCAB_MODE_ROWS;  // largest M with W as the A operand
 constexpr int kMaxStages = 16;
 constexpr int kMaxShards = 1024;  // largest k (the combine keeps k shard records in smem)
-#ifndef SB_ROWS_CLUSTER
-#define SB_ROWS_CLUSTER 2
-#endif
-constexpr int kRowsCluster = SB_ROWS_CLUSTER;  // rows mode: CTAs (consecutive M tiles) per W tile
-#ifndef SB_ROWS_PAIR
-#define SB_ROWS_PAIR 1
-#endif
-// rows mode with 2-CTA clusters: one cta_group::2 MMA per pair (each CTA stages half of the
-// W tile) instead of a cta_group::1 MMA per CTA on a multicast copy of the whole W tile
-constexpr bool kRowsPair = SB_ROWS_PAIR != 0 && SB_ROWS_CLUSTER == 2;
+// rows mode: a cluster of two CTAs (consecutive M tiles) shares each W tile; one
+// cta_group::2 MMA per pair, each CTA staging its own half of the W tile
+constexpr int kRowsCluster = 2;
 
 constexpr int kEpiWarps = 8;         // two epilogue warps per TMEM lane quadrant
 constexpr int kFirstEpiWarp = 3;     // warps 0 and 2 load, warp 1 issues MMAs + owns TMEM

@@ -71,19 +71,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *t
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar_cluster), "r"(c0), "r"(c1), "l"(policy)
         : "memory");
 }
-// Multicast variant: the box lands at the same shared-memory offset in every CTA of the
-// cluster named in cta_mask, and completes bytes on the mbarrier at the same offset in each.
-__device__ __forceinline__ void tma_load_2d_mc(void *dst, const CUtensorMap *tm, uint64_t *bar,
-                                               int32_t c0, int32_t c1, uint16_t cta_mask,
-                                               uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(
-            smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(cta_mask),
-        "l"(policy)
-        : "memory");
-}
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -138,16 +125,6 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
-        : "memory");
-}
-
-// As umma_commit, but the arrival is delivered to the mbarrier at the same shared-memory
-// offset in every CTA of the cluster named in cta_mask.
-__device__ __forceinline__ void umma_commit_mc(uint64_t *bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_u32(bar)),
-        "h"(cta_mask)
         : "memory");
 }
 
@@ -293,7 +270,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-// Monotone map float -> uint32 (ascending floats give ascending integers; no NaNs).
 // Mask of the lanes below this one in the warp.
 __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
@@ -301,6 +277,7 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
+// Monotone map float -> uint32 (ascending floats give ascending integers; no NaNs).
 __device__ __forceinline__ uint32_t float_to_ordered(float f) {
     uint32_t u = __float_as_uint(f);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
