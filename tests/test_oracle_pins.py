@@ -312,6 +312,23 @@ def test_payload_closed_form_against_pages():
     assert round(g["r0_bytes_per_step"] / g["p0_bytes_per_step"]) == g["p0_ratio"]
 
 
+def test_payload_token_and_token_logprob_sizes():
+    """Token surface: Figure 2(b)'s 256 B per decode step are four lane frames of 16 rows
+    (concurrency 16), one int32 token per row in each, so 4 B per row.  Token + chosen
+    log-prob adds one fp32 per row: int32 + float32 = 8 B, a reduction of 1 - 4/V against
+    bf16 logits, still above the pages' 'more than 99.97%' at both vocabularies."""
+    g = {r[0]: float(r[1]) for r in _read_golden("payload_pages.txt")}
+    assert oracle.payload_bytes_per_row(0, 151936) == g["p0_bytes_per_step"] / (4 * 16)
+    want = np.dtype(np.int32).itemsize + np.dtype(np.float32).itemsize
+    for V in (4096, 151936, 200064):
+        assert oracle.payload_bytes_per_row(1, V) == want == 8
+        red = 1.0 - oracle.payload_bytes_per_row(1, V) / oracle.payload_bytes_per_row(2, V)
+        assert abs(red - (1.0 - 4.0 / V)) < 1e-15
+        if V > 4096:
+            assert red > g["min_traffic_reduction"]
+    assert np.isnan(oracle.payload_bytes_per_row(3, 151936))
+
+
 # ---------------------------------------------------------------- top-K log-prob surface
 @pytest.mark.parametrize("K", [1, 3, 7])
 def test_topk_bruteforce_on_exact_logits(K):

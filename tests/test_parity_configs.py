@@ -2,9 +2,10 @@
 
 Each workload draws its inputs on the GPU (seed 0; targets seed 1) and runs the projection
 once through the C ABI.  Rows the fp64 oracle can afford are compared element by element
-(all rows for the two decode shapes; a fixed sample spread over tiles for prefill scoring and
-sampling); every row is also checked against torch's fp32 matmul + logsumexp (a library
-routine, used here as a second reference that scales to every row).
+(every row of the two decode shapes and of the 256-row sampling batch; a fixed sample spread
+over the M tiles for prefill scoring); every row is also checked against torch's fp32 matmul
++ logsumexp (a library routine, used here as a second reference that scales to every row),
+including the target log-prob of each of the 4096 prefill rows.
 """
 import numpy as np
 import pytest
@@ -24,8 +25,9 @@ def _built():
     __graft_entry__.build()
 
 
-def _library_reference_check(H, W, res, *, T=1.0, lse_only=False):
-    """All rows: tokens and logsumexp against torch fp32 (tf32 off) on the GPU."""
+def _library_reference_check(H, W, res, *, T=1.0, lse_only=False, targets=None):
+    """All rows: tokens, logsumexp and (given targets) the target log-prob against torch
+    fp32 (tf32 off) on the GPU."""
     prev = torch.backends.cuda.matmul.allow_tf32
     torch.backends.cuda.matmul.allow_tf32 = False
     try:
@@ -35,6 +37,9 @@ def _library_reference_check(H, W, res, *, T=1.0, lse_only=False):
             y = z / T
             lse = torch.logsumexp(y, dim=1)
             assert float((res["lse"][r0:r0 + 512] - lse).abs().max()) <= TOL
+            if targets is not None:
+                tl = z.gather(1, targets[r0:r0 + 512].long()[:, None])[:, 0] - lse
+                assert float((res["target_logprob"][r0:r0 + 512] - tl).abs().max()) <= TOL
             if lse_only:
                 continue
             top2 = torch.topk(z, 2, dim=1).values
@@ -85,7 +90,8 @@ def test_decode64_full_logits_vs_token():
 
 def test_prefill_scoring_lse_and_target_logprob():
     """M=4096, d=6144, V=200064, k=4 (S=50016): lse + target log-prob, no logits written.
-    Oracle on 12 rows spread over the M tiles (first, last, tile edges); torch on all."""
+    Oracle on 12 rows spread over the M tiles (first, last, tile edges); torch on all rows,
+    target log-probs included."""
     M, d, V, k = 4096, 6144, 200064, 4
     H, W = synth.make_hw(M, d, V, seed=0, device="cuda")
     tg = synth.make_targets(M, V, seed=1, device="cuda")
@@ -95,19 +101,18 @@ def test_prefill_scoring_lse_and_target_logprob():
     rows = [0, 1, 127, 128, 255, 1000, 2047, 2048, 3001, 3967, 4094, 4095]
     ref = _oracle(H, W, k, rows, targets=tg.cpu().numpy()[rows])
     check_rows(res, ref, rows, check_targets=True)
-    _library_reference_check(H, W, res)
+    _library_reference_check(H, W, res, targets=tg)
 
 
 def test_sampling_gumbel_token():
-    """M=256, d=5120, V=151936, k=4: GUMBEL_TOKEN at T=0.7 with seed 1234; oracle on 24 rows
-    (tokens by the candidate rule on the Gumbel key, tempered lse and log-prob)."""
+    """M=256, d=5120, V=151936, k=4: GUMBEL_TOKEN at T=0.7 with seed 1234; the oracle on
+    every row (tokens by the candidate rule on the Gumbel key, tempered lse and log-prob)."""
     M, d, V, k, T, seed = 256, 5120, 151936, 4, 0.7, 1234
     H, W = synth.make_hw(M, d, V, seed=0, device="cuda")
     res = sb.project(H, W, k, sb.SB_GUMBEL_TOKEN, temperature=T, seed=seed)
     torch.cuda.synchronize()
     assert sb.sb_last_device_status(res["_outputs"]) == sb.SB_OK
-    rows = [0, 1, 15, 16, 31, 63, 64, 100, 127, 128, 129, 150, 170, 191, 192, 200, 223, 224,
-            230, 240, 250, 253, 254, 255]
+    rows = list(range(M))
     ref = _oracle(H, W, k, rows, gumbel=True, temperature=np.float32(T).item(), seed=seed)
     check_rows(res, ref, rows, gumbel=True, T=np.float32(T).item(), seed=seed)
     _library_reference_check(H, W, res, T=np.float32(T).item(), lse_only=True)
