@@ -74,6 +74,8 @@ def lib():
         L.sb_lmhead_records.restype = i32
         L.sb_lmhead_project_static_scratch.argtypes = L.sb_lmhead_project.argtypes
         L.sb_lmhead_project_static_scratch.restype = i32
+        L.sb_static_scratch_last_status.argtypes = []
+        L.sb_static_scratch_last_status.restype = i32
         L.sb_lmhead_project_from_host.argtypes = [P, P, P, i64, i64, i64, i32, i32,
                                                   ctypes.c_float, u64,
                                                   ctypes.POINTER(sb_outputs), P, P, P]
@@ -110,6 +112,8 @@ def lib():
         L.sb_status_string.restype = ctypes.c_char_p
         L.sb_device_info.argtypes = [ctypes.POINTER(i32), ctypes.POINTER(i32)]
         L.sb_device_info.restype = i32
+        L.sb_debug_combine_math.argtypes = [i32, P, P, i64, P]
+        L.sb_debug_combine_math.restype = i32
         L.sb_debug_gumbel_from_bits.argtypes = [P, P, i64, P]
         L.sb_debug_gumbel_from_bits.restype = i32
         L.sb_debug_configure.argtypes = [i32, u64]
@@ -228,6 +232,11 @@ def sb_lmhead_project_static_scratch(H, W, M, d, V, k, surface, temperature, see
                                                       ctypes.byref(out), _stream(stream)))
 
 
+def sb_static_scratch_last_status() -> int:
+    """Device status of the last static-scratch call on the current device (synchronises)."""
+    return int(lib().sb_static_scratch_last_status())
+
+
 def sb_combine_shard_records(workspace, M, k, tiles_per_shard, surface, temperature,
                              out: sb_outputs, stream=None) -> int:
     return int(lib().sb_combine_shard_records(_ptr(workspace), M, k, tiles_per_shard,
@@ -310,6 +319,11 @@ def sb_device_info():
 
 def sb_debug_gumbel_from_bits(bits, g, count: int, stream=None) -> int:
     return int(lib().sb_debug_gumbel_from_bits(_ptr(bits), _ptr(g), int(count), _stream(stream)))
+
+
+def sb_debug_combine_math(op: int, x, y, count: int, stream=None) -> int:
+    return int(lib().sb_debug_combine_math(int(op), _ptr(x), _ptr(y), int(count),
+                                           _stream(stream)))
 
 
 def sb_debug_configure(stall_epilogue: bool, wait_limit_ns: int) -> int:

@@ -66,3 +66,15 @@ extern "C" int32_t sb_lmhead_project_static_scratch(const void *H, const void *W
     o.workspace_bytes = kSbStaticScratchBytes;
     return sb_lmhead_project(H, W, M, d, V, k, surface, temperature, seed, &o, stream);
 }
+
+// The device status of the last static-scratch call on the current device: its status
+// word sits in the array's header, which the caller cannot address, so it is read here
+// through the looked-up address, as sb_last_device_status reads a caller's workspace.
+extern "C" int32_t sb_static_scratch_last_status(void) {
+    void *scratch = nullptr;
+    if (int32_t e = scratch_address(&scratch)) return e;
+    sb_outputs o{};
+    o.workspace = scratch;
+    o.workspace_bytes = kSbStaticScratchBytes;
+    return sb_last_device_status(&o);
+}

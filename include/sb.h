@@ -264,13 +264,33 @@ int32_t sb_combine_shard_records(const void *workspace, int64_t M, int32_t k,
  *   Every call on a device shares the one array and leaves its records there; nothing in
  *   it needs clearing between calls, but calls that overlap on the GPU (different streams,
  *   or host threads without ordering) race on it and give undefined results.
- *   The device status word also lives in the array, so a device-side timeout of this call
- *   is not reported (sb_last_device_status cannot reach it).
+ *   The device status word also lives in the array, out of the caller's reach: read it with
+ *   sb_static_scratch_last_status() (not sb_last_device_status) after synchronising.  Both
+ *   errors found on the device land there: a bounded wait that ran out
+ *   (SB_ERR_DEVICE_TIMEOUT) and a scoring target outside [0, V) (SB_ERR_INVALID_ARG).
  */
 int32_t sb_lmhead_project_static_scratch(const void *H, const void *W, int64_t M, int64_t d,
                                          int64_t V, int32_t k, int32_t surface,
                                          float temperature, uint64_t seed,
                                          const sb_outputs *out, void *stream);
+
+/*
+ * The device status of the last sb_lmhead_project_static_scratch call on the current device
+ * (no paper counterpart): SB_OK, SB_ERR_DEVICE_TIMEOUT or SB_ERR_INVALID_ARG, as
+ * sb_last_device_status reports for a caller's workspace; SB_ERR_CUDA if the array cannot be
+ * read.  Synchronises with the device (a blocking device-to-host copy of 16 bytes into host
+ * stack memory; allocates nothing).  Call it after the static-scratch call has completed and
+ * before the next one is enqueued.
+ */
+int32_t sb_static_scratch_last_status(void);
+
+/* Test hook: the two functions of the record merge, as the combine kernels evaluate them,
+ * on count entries of device arrays (enqueued on stream): op 0 gives y[i] = e^x[i] for
+ * x <= 0 (the hardware base-2 exponential of x * log2(e), the product rounded to fp32);
+ * op 1 gives y[i] = ln x[i].  With these two, a host restatement of the merge order in
+ * fp32 reproduces sb_combine_shard_records bit for bit. */
+int32_t sb_debug_combine_math(int32_t op, const float *x, float *y, int64_t count,
+                              void *stream);
 
 /* Test hook: g[i] = the Gumbel noise the projection kernels derive from the 24-bit
  * uniform bits[i] & 0xFFFFFF (u = bits * 2^-24), for count entries of device arrays,
