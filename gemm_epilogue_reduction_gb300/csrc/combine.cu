@@ -19,41 +19,11 @@
 // The output bits are therefore a function of the record bits alone (any grid, any run).
 #include <climits>
 
+#include "sb_combine_math.cuh"
 #include "sb_internal.h"
 
 namespace sb {
 namespace {
-
-struct Rec {
-    float m;
-    int i;
-    float s;
-};
-struct GRec {
-    float k;
-    int i;
-    float z;
-};
-
-__device__ __forceinline__ float exp_nonpos(float x) {  // e^x for x <= 0 (2 ulp)
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * 1.4426950408889634f));
-    return y;
-}
-
-__device__ __forceinline__ Rec merge(const Rec &a, const Rec &b) {
-    Rec r;
-    r.m = fmaxf(a.m, b.m);
-    r.i = (a.m > b.m) ? a.i : ((b.m > a.m) ? b.i : min(a.i, b.i));
-    const float sa = (a.m == -INFINITY) ? 0.f : a.s * exp_nonpos(a.m - r.m);
-    const float sb = (b.m == -INFINITY) ? 0.f : b.s * exp_nonpos(b.m - r.m);
-    r.s = sa + sb;
-    return r;
-}
-
-__device__ __forceinline__ GRec gmerge(const GRec &a, const GRec &b) {
-    return (a.k > b.k || (a.k == b.k && a.i < b.i)) ? a : b;
-}
 
 constexpr int kMaxWarps = 8;
 constexpr int kBatch = 16;  // records each lane loads before folding them
@@ -161,9 +131,9 @@ __global__ void __launch_bounds__(32 * kMaxWarps) combine_kernel(const CombinePa
         acc = merge(acc, Rec{sm[s2], si[s2], ss[s2]});
         if (GUMBEL) gacc = gmerge(gacc, GRec{sgk[s2], sgi[s2], sgz[s2]});
     }
-    const float lse = acc.m + logf(acc.s);
+    const float lse = row_lse(acc);
     const int tok = GUMBEL ? gacc.i : acc.i;
-    const float tlp = GUMBEL ? gacc.z * p.inv_t - lse : -logf(acc.s);
+    const float tlp = GUMBEL ? tempered_minus(gacc.z, p.inv_t, lse) : -log_sum(acc.s);
     p.token[row] = tok;
     if (p.lse) p.lse[row] = lse;
     if (p.token_logprob) p.token_logprob[row] = tlp;
@@ -171,7 +141,7 @@ __global__ void __launch_bounds__(32 * kMaxWarps) combine_kernel(const CombinePa
     if (p.token_logprob_host) p.token_logprob_host[row] = tlp;
     if (p.target_logprob) {
         const float tz = p.ws.tz[row];
-        p.target_logprob[row] = (GUMBEL ? tz * p.inv_t : tz) - lse;
+        p.target_logprob[row] = GUMBEL ? tempered_minus(tz, p.inv_t, lse) : __fsub_rn(tz, lse);
     }
 }
 
@@ -233,10 +203,11 @@ __global__ void merge_payload_kernel(const CombineParams c, const unsigned char 
         acc = merge(acc, Rec{f[0], i[1], f[2]});
         if (GUMBEL) gacc = gmerge(gacc, GRec{f[3], i[4], f[5]});
     }
-    const float lse = acc.m + logf(acc.s);
+    const float lse = row_lse(acc);
     c.token[row] = GUMBEL ? gacc.i : acc.i;
     if (c.lse) c.lse[row] = lse;
-    if (c.token_logprob) c.token_logprob[row] = GUMBEL ? gacc.z * c.inv_t - lse : -logf(acc.s);
+    if (c.token_logprob)
+        c.token_logprob[row] = GUMBEL ? tempered_minus(gacc.z, c.inv_t, lse) : -log_sum(acc.s);
 }
 
 // ------------------------------------------------------------------ top-K helpers
@@ -428,7 +399,7 @@ __global__ void __launch_bounds__(32 * kMaxWarps) combine_topk_kernel(const Comb
 
     Rec acc{-INFINITY, INT_MAX, 0.f};
     for (int s2 = 0; s2 < p.k; ++s2) acc = merge(acc, Rec{sm[s2], si[s2], ss[s2]});
-    const float lse = acc.m + logf(acc.s);
+    const float lse = row_lse(acc);
     if (lane < K) {
         p.topk_ids[static_cast<size_t>(row) * K + lane] = wli[lane];
         p.topk_logprob[static_cast<size_t>(row) * K + lane] = wlv[lane] - lse;
@@ -436,10 +407,10 @@ __global__ void __launch_bounds__(32 * kMaxWarps) combine_topk_kernel(const Comb
     if (lane != 0) return;
     p.token[row] = acc.i;
     if (p.lse) p.lse[row] = lse;
-    if (p.token_logprob) p.token_logprob[row] = -logf(acc.s);
+    if (p.token_logprob) p.token_logprob[row] = -log_sum(acc.s);
     if (p.token_host) p.token_host[row] = acc.i;
-    if (p.token_logprob_host) p.token_logprob_host[row] = -logf(acc.s);
-    if (p.target_logprob) p.target_logprob[row] = p.ws.tz[row] - lse;
+    if (p.token_logprob_host) p.token_logprob_host[row] = -log_sum(acc.s);
+    if (p.target_logprob) p.target_logprob[row] = __fsub_rn(p.ws.tz[row], lse);
 }
 
 }  // namespace
