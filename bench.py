@@ -320,17 +320,145 @@ def run_reference(args, cfg, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def run_partial(args, cfg, world, rank, local):
-    """The row-parallel partial completion (lane partials + their ordered sum); under
-    torchrun each rank runs its own replica (weak scaling, max-over-ranks timing)."""
+def make_projection(cfg, rank=0):
+    """Inputs (seed 0; targets seed 1; rank r > 0 draws its own rows), caller-owned outputs
+    and the three step closures of one projection workload on the current device."""
+    import types
     import torch
-    import torch.distributed as dist
     import gemm_epilogue_reduction_gb300 as sb
-    from gemm_epilogue_reduction_gb300 import build as sbbuild, synth
-    sbbuild.build()
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from gemm_epilogue_reduction_gb300 import synth
+    M, d, V, k = cfg["M"], cfg["d"], cfg["V"], cfg["k"]
+    w = types.SimpleNamespace(M=M, d=d, V=V, k=k, surface=sb.SURFACES[cfg["surface"]],
+                              T=cfg.get("T", 1.0), gseed=cfg.get("seed", 0))
+    w.H, w.W = synth.make_hw(M, d, V, seed=0, device="cuda")
+    if rank:
+        w.H = synth.make_hw(M, d, 1, seed=rank_rows_seed(rank), device="cuda")[0]
+    w.targets = synth.make_targets(M, V, seed=1, device="cuda") if cfg.get("targets") else None
+    w.out, w.bufs = sb.make_outputs(M, V, k, w.surface, targets=w.targets,
+                                    topk=cfg.get("topk", 0))
+    w.tps = sb.sb_tiles_per_shard(M, V, k)
+    w.stream = torch.cuda.current_stream()
+
+    def records():
+        st = sb.sb_lmhead_records(w.H, w.W, M, d, V, k, w.surface, w.T, w.gseed, w.out, w.stream)
+        if st != sb.SB_OK:
+            raise sb.SbError(st, "sb_lmhead_records")
+
+    def combine():
+        st = sb.sb_combine_shard_records(w.bufs["workspace"], M, k, w.tps, w.surface, w.T, w.out,
+                                         w.stream)
+        if st != sb.SB_OK:
+            raise sb.SbError(st, "sb_combine_shard_records")
+
+    def project():
+        st = sb.sb_lmhead_project(w.H, w.W, M, d, V, k, w.surface, w.T, w.gseed, w.out, w.stream)
+        if st != sb.SB_OK:
+            raise sb.SbError(st, "sb_lmhead_project")
+
+    w.records, w.combine, w.project = records, combine, project
+    w.in_bytes = V * d * 2 + M * d * 2
+    return w
+
+
+def kernel_times(w, K):
+    """Average ms of the GEMM kernel alone and of the combine alone: K launches each, CUDA
+    events around every launch on the launching stream."""
+    import torch
+    evk = [torch.cuda.Event(enable_timing=True) for _ in range(2 * K)]
+    res = []
+    for fn in (w.records, w.combine):
+        for i in range(K):
+            evk[2 * i].record(w.stream)
+            fn()
+            evk[2 * i + 1].record(w.stream)
+        torch.cuda.synchronize()
+        res.append(sum(evk[2 * i].elapsed_time(evk[2 * i + 1]) for i in range(K)) / K)
+    return res[0], res[1]
+
+
+def projection_roofline(w, gemm_ms, comb_ms, peaks, peak_src, tensor_bound, traffic=None):
+    """Roofline of the GEMM kernel: algorithmic bytes (W and H read once, 12 B of outputs per
+    row, bf16 logits for FULL_LOGITS) or flops (2 M V d) over its event-timed duration."""
+    import gemm_epilogue_reduction_gb300 as sb
+    M, d, V = w.M, w.d, w.V
+    alg_bytes = V * d * 2 + M * d * 2 + M * 12 + (M * V * 2 if w.surface == sb.SB_FULL_LOGITS
+                                                   else 0)
+    alg_flops = 2.0 * M * V * d
+    gbs = alg_bytes / (gemm_ms * 1e-3) / 1e9
+    tfs = alg_flops / (gemm_ms * 1e-3) / 1e12
+    if not tensor_bound:
+        return {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / peaks["hbm_gbs"], "traffic": traffic,
+                "peak_source": f"{peak_src} (HBM copy, burst)", "kernel": "lmhead_kernel",
+                "kernel_ms": gemm_ms, "combine_ms": comb_ms, "algorithmic_bytes": alg_bytes,
+                "tensor_tflops": tfs,
+                "tensor_frac": tfs / peaks["bf16_tflops"],
+                "nominal": {"peak": NOMINAL_PEAKS["hbm_gbs"],
+                            "frac": gbs / NOMINAL_PEAKS["hbm_gbs"]}}
+    sus = peaks.get("bf16_tflops_sustained")
+    return {"bound": "tensor", "achieved": tfs, "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": tfs / peaks["bf16_tflops"], "traffic": traffic,
+            "peak_source": f"{peak_src} (cuBLAS bf16, burst)", "kernel": "lmhead_kernel",
+            "kernel_ms": gemm_ms, "combine_ms": comb_ms, "algorithmic_flops": alg_flops,
+            "hbm_gbs": gbs,
+            "sustained": ({"peak": sus, "frac": tfs / sus} if sus else None),
+            "nominal": {"peak": NOMINAL_PEAKS["bf16_tflops"],
+                        "frac": tfs / NOMINAL_PEAKS["bf16_tflops"]}}
+
+
+def steps_for(step, stream, seconds, lo=5, hi=4000, flush=None):
+    """Steps that fill about `seconds` of device time (from three timed steps)."""
+    est = timed_steps(step, 3, stream, flush)
+    return max(lo, min(hi, int(seconds * 1e3 / max(est, 1e-3))))
+
+
+def measure_workload(name, seconds, peaks, peak_src, gpu_index):
+    """One workload of the per-configuration table: back-to-back projection steps for about
+    `seconds` (clocks sampled meanwhile), then each kernel alone."""
+    import torch
+    import gemm_epilogue_reduction_gb300 as sb
+    cfg = WORKLOADS[name]
+    w = make_projection(cfg)
+    flush = L2Flush() if w.in_bytes < l2_bytes() else None
+    for _ in range(3):
+        w.project()
+    torch.cuda.synchronize()
+    if sb.sb_last_device_status(w.out) != sb.SB_OK:
+        raise RuntimeError(f"{name}: device status not OK after warm-up")
+    K = steps_for(w.project, w.stream, seconds, flush=flush)
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_index) as clocks:
+        step_ms = timed_steps(w.project, K, w.stream, flush)
+    if sb.sb_last_device_status(w.out) != sb.SB_OK:
+        raise RuntimeError(f"{name}: device status not OK after the timed steps")
+    gemm_ms, comb_ms = kernel_times(w, min(K, 200))
+    roof = projection_roofline(w, gemm_ms, comb_ms, peaks, peak_src,
+                               tensor_bound=name.startswith("prefill"))
+    entry = {"desc": cfg["desc"], "surface": cfg["surface"], "steps": K,
+             "step_us": step_ms * 1e3, "rows_per_s": w.M / (step_ms * 1e-3),
+             "gemm_us": gemm_ms * 1e3, "combine_us": comb_ms * 1e3,
+             "bound": roof["bound"], "frac": roof["frac"], "achieved": roof["achieved"],
+             "unit": roof["unit"], "clocks": clocks.summary()}
+    if roof["bound"] == "tensor":
+        entry["frac_sustained"] = roof["sustained"]["frac"] if roof["sustained"] else None
+        entry["hbm_gbs"] = roof["hbm_gbs"]
+    else:
+        entry["tensor_frac"] = roof["tensor_frac"]
+        entry["nominal_frac"] = roof["nominal"]["frac"]
+    entry["payload_bytes"] = sb.sb_payload_bytes(w.M, w.k, w.surface) if w.surface in (
+        sb.SB_TOKEN, sb.SB_TOKEN_LOGPROB, sb.SB_GUMBEL_TOKEN) else None
+    del w
+    torch.cuda.empty_cache()
+    return entry
+
+
+def measure_partial(name, seconds, peaks, peak_src, gpu_index, steps=None, warmup=3):
+    """The row-parallel partial completion (both kernels) timed back to back; returns
+    (ms per call, roofline dict, clocks summary)."""
+    import torch
+    import gemm_epilogue_reduction_gb300 as sb
+    from gemm_epilogue_reduction_gb300 import synth
+    cfg = WORKLOADS[name]
     M, N, K, lanes = cfg["M"], cfg["N"], cfg["K"], cfg["lanes"]
     X, W = synth.make_hw(M, K, N, seed=0, device="cuda")
     nbytes = sb.sb_partial_workspace_bytes(M, N, K, lanes)
@@ -343,40 +471,120 @@ def run_partial(args, cfg, world, rank, local):
         if st != sb.SB_OK:
             raise sb.SbError(st, "sb_partial_completion")
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
-    K_ = args.steps
     in_bytes = N * K * 2 + M * K * 2
     flush = L2Flush() if in_bytes < l2_bytes() else None
-    if world > 1:
-        dist.barrier()
+    n = steps if steps else steps_for(step, stream, seconds, flush=flush)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        ms = timed_steps(step, K_, stream, flush)
+    with ClockSampler(gpu_index) as clocks:
+        ms = timed_steps(step, n, stream, flush)
+    alg = N * K * 2 + M * K * 2 + M * N * 2
+    ach = alg / (ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": ach / peaks["hbm_gbs"], "traffic": None,
+            "peak_source": f"{peak_src} (HBM copy, burst)",
+            "kernel": "partial_kernel + complete_kernel", "algorithmic_bytes": alg,
+            "nominal": {"peak": NOMINAL_PEAKS["hbm_gbs"], "frac": ach / NOMINAL_PEAKS["hbm_gbs"]}}
+    flushed = flush is not None
+    del X, W, ws, Y, flush
+    torch.cuda.empty_cache()
+    return ms, n, roof, clocks.summary(), in_bytes, flushed
+
+
+# Links for the Equation (7) decision: the pages' 1-GbE testbed, a PCIe-class host link and an
+# NVLink-class device link (payload bytes per second).
+SELECTION_LINKS = {"1GbE": 1e9 / 8, "25GB/s": 25e9, "900GB/s": 900e9}
+
+
+def plan_selection(M, V, k, local_proj_s, local_ref_s, frame_startup_s=0.0):
+    """Equation (7) on measured local costs: plan r ships the complete bf16 logits (one frame
+    per lane, 2 M V bytes), plan s each lane's shard-local projection record (one frame per
+    lane, sb_payload_bytes of the token surface); L_s and L_r are the two plans' measured
+    on-device step times.  Returns the decision per link and the threshold bandwidth (the
+    link rate above which the complete logits would win: (B_r - B_s) / (L_s - L_r), or None
+    when projecting costs no more on the device, so that it wins on every link)."""
+    import gemm_epilogue_reduction_gb300 as sb
+    B_r = 2.0 * M * V
+    B_s = float(sb.sb_payload_bytes(M, k, sb.SB_TOKEN))
+    F_r = F_s = float(k)
+    out = {"bytes_ref": B_r, "bytes_proj": B_s, "frames_ref": F_r, "frames_proj": F_s,
+           "local_proj_s": local_proj_s, "local_ref_s": local_ref_s,
+           "frame_startup_s": frame_startup_s, "decisions": {}}
+    for nm, beta in SELECTION_LINKS.items():
+        dcs, margin = sb.sb_select_source_projection(B_r, B_s, F_r, F_s, beta, frame_startup_s,
+                                                     local_proj_s, local_ref_s)
+        out["decisions"][nm] = {"link_bytes_per_s": beta, "project": dcs,
+                                "margin_s": margin}
+    dl = local_proj_s - local_ref_s - frame_startup_s * (F_r - F_s)
+    out["threshold_bytes_per_s"] = (B_r - B_s) / dl if dl > 0 else None
+    return out
+
+
+def measure_plan_costs(seconds, peaks, peak_src, gpu_index, ref="decode64",
+                       proj="decode64_token"):
+    """L_r and L_s of Equation (7) at a decode shape, measured on this device: the step time
+    of the complete-logit surface and of the projected token surface on the same shape."""
+    er = measure_workload(ref, seconds, peaks, peak_src, gpu_index)
+    es = measure_workload(proj, seconds, peaks, peak_src, gpu_index)
+    c = WORKLOADS[ref]
+    sel = plan_selection(c["M"], c["V"], c["k"], es["step_us"] * 1e-6, er["step_us"] * 1e-6)
+    sel["shape"] = {"M": c["M"], "d": c["d"], "V": c["V"], "k": c["k"]}
+    sel["surfaces"] = {"ref": er["surface"], "proj": es["surface"]}
+    return sel, er, es
+
+
+PER_CONFIG = ("decode64", "decode64_token", "prefill", "sampling")
+
+
+def per_config_table(seconds, peaks, peak_src, gpu_index):
+    """The other configurations, each timed on its own for about `seconds`, plus the partial
+    completion and the Equation (7) decision on the measured decode64 costs."""
+    out = {}
+    sel, out["decode64"], out["decode64_token"] = measure_plan_costs(seconds, peaks, peak_src,
+                                                                     gpu_index)
+    for name in PER_CONFIG[2:]:
+        out[name] = measure_workload(name, seconds, peaks, peak_src, gpu_index)
+    ms, n, roof, clk, _, _ = measure_partial("mlp_down", seconds, peaks, peak_src, gpu_index)
+    out["mlp_down"] = {"desc": WORKLOADS["mlp_down"]["desc"], "steps": n, "step_us": ms * 1e3,
+                       "rows_per_s": WORKLOADS["mlp_down"]["M"] / (ms * 1e-3),
+                       "bound": "hbm", "frac": roof["frac"], "achieved": roof["achieved"],
+                       "unit": "GB/s", "nominal_frac": roof["nominal"]["frac"], "clocks": clk}
+    out["selection"] = sel
+    return out
+
+
+def run_partial(args, cfg, world, rank, local):
+    """The row-parallel partial completion (lane partials + their ordered sum); under
+    torchrun each rank runs its own replica (weak scaling, max-over-ranks timing)."""
+    import torch
+    import torch.distributed as dist
+    from gemm_epilogue_reduction_gb300 import build as sbbuild
+    sbbuild.build()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist.barrier()
+    peaks, peak_src = load_peaks()
+    ms, K_, roof, clk, in_bytes, flushed = measure_partial(
+        args.workload, 0, peaks, peak_src, local, steps=args.steps, warmup=args.warmup)
     if world > 1:
         dist.barrier()
     ms = max_over_ranks(ms, "cuda")
-    peaks, peak_src = load_peaks()
-    alg = N * K * 2 + M * K * 2 + M * N * 2
-    ach = alg / (ms * 1e-3) / 1e9
+    M = cfg["M"]
     line = {
         "metric": METRIC, "value": job_rows_per_s(world, M, ms), "unit": "rows/s", "n_gpus": world,
         "steps": K_, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "M": M, "N": N, "K": K, "lanes": lanes,
-                   "desc": cfg["desc"],
+        "config": {"workload": args.workload, "M": M, "N": cfg["N"], "K": cfg["K"],
+                   "lanes": cfg["lanes"], "desc": cfg["desc"],
                    "l2": ("inputs %.0f MB > L2, streamed every step" % (in_bytes / 1e6))
-                   if flush is None else
+                   if not flushed else
                    ("inputs %.0f MB fit in L2: L2 flushed (2x L2 written) before every "
                     "step, outside its events" % (in_bytes / 1e6))},
-        "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": ach / peaks["hbm_gbs"], "traffic": None,
-                     "peak_source": f"{peak_src} (HBM copy, burst)",
-                     "kernel": "partial_kernel + complete_kernel", "algorithmic_bytes": alg,
-                     "nominal": {"peak": NOMINAL_PEAKS["hbm_gbs"],
-                                 "frac": ach / NOMINAL_PEAKS["hbm_gbs"]}},
-        "cpu_baseline": None, "e2e": None, "clocks": clocks.summary(), "gpu_launches": 2 * K_,
+        "roofline": roof,
+        "cpu_baseline": None, "e2e": None, "clocks": clk, "gpu_launches": 2 * K_,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -394,6 +602,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--per-config-seconds", type=float, default=0.4,
+                    help="device seconds of back-to-back steps per entry of the per_config "
+                         "table (N = 1, default workload only; 0 leaves the table out)")
     args = ap.parse_args()
     cfg = WORKLOADS[args.workload]
     world, rank, local = dist_env()
@@ -417,36 +628,14 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
-    M, d, V, k = cfg["M"], cfg["d"], cfg["V"], cfg["k"]
-    surface = sb.SURFACES[cfg["surface"]]
-    T = cfg.get("T", 1.0)
-    gseed = cfg.get("seed", 0)
     # each rank draws its own batch of rows (weak scaling) and the same W
-    H, W = synth.make_hw(M, d, V, seed=0, device="cuda")
-    if rank:
-        H = synth.make_hw(M, d, 1, seed=rank_rows_seed(rank), device="cuda")[0]
-    targets = synth.make_targets(M, V, seed=1, device="cuda") if cfg.get("targets") else None
-    out, bufs = sb.make_outputs(M, V, k, surface, targets=targets, topk=cfg.get("topk", 0))
-    Tps = sb.sb_tiles_per_shard(M, V, k)
-    stream = torch.cuda.current_stream()
-
-    def step_records():
-        st = sb.sb_lmhead_records(H, W, M, d, V, k, surface, T, gseed, out, stream)
-        if st != sb.SB_OK:
-            raise sb.SbError(st, "sb_lmhead_records")
-
-    def step_combine():
-        st = sb.sb_combine_shard_records(bufs["workspace"], M, k, Tps, surface, T, out, stream)
-        if st != sb.SB_OK:
-            raise sb.SbError(st, "sb_combine_shard_records")
-
-    def step_project():
-        st = sb.sb_lmhead_project(H, W, M, d, V, k, surface, T, gseed, out, stream)
-        if st != sb.SB_OK:
-            raise sb.SbError(st, "sb_lmhead_project")
+    w = make_projection(cfg, rank)
+    M, d, V, k = w.M, w.d, w.V, w.k
+    H, W, out, stream = w.H, w.W, w.out, w.stream
+    surface, T, gseed = w.surface, w.T, w.gseed
 
     for _ in range(args.warmup):
-        step_project()
+        w.project()
     torch.cuda.synchronize()
     if sb.sb_last_device_status(out) != sb.SB_OK:
         raise RuntimeError("device status not OK after warm-up")
@@ -455,14 +644,13 @@ def main():
     # as a programmatic dependent launch, and each call's GEMM the previous call's combine),
     # one event before the first step and one after the last
     K = args.steps
-    in_bytes = V * d * 2 + M * d * 2
-    flush = L2Flush() if in_bytes < l2_bytes() else None
+    flush = L2Flush() if w.in_bytes < l2_bytes() else None
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         t_wall = time.perf_counter()
-        total_ms = timed_steps(step_project, K, stream, flush) * K
+        total_ms = timed_steps(w.project, K, stream, flush) * K
         t_wall = time.perf_counter() - t_wall
     if world > 1:
         dist.barrier()
@@ -471,19 +659,7 @@ def main():
         raise RuntimeError("device status not OK after the timed region")
 
     # ---- per-kernel durations: each kernel alone, K launches, events around each launch
-    evk = [torch.cuda.Event(enable_timing=True) for _ in range(2 * K)]
-    for i in range(K):
-        evk[2 * i].record(stream)
-        step_records()
-        evk[2 * i + 1].record(stream)
-    torch.cuda.synchronize()
-    gemm_ms = [evk[2 * i].elapsed_time(evk[2 * i + 1]) for i in range(K)]
-    for i in range(K):
-        evk[2 * i].record(stream)
-        step_combine()
-        evk[2 * i + 1].record(stream)
-    torch.cuda.synchronize()
-    comb_ms = [evk[2 * i].elapsed_time(evk[2 * i + 1]) for i in range(K)]
+    gemm_avg, comb_avg = kernel_times(w, K)
 
     # ---- end to end through the public call with host buffers: H is copied from pinned
     # host memory and token + log-prob are copied back inside the call, every step
@@ -531,32 +707,11 @@ def main():
 
     ms_per_step = total_ms / K
     value = job_rows_per_s(world, M, ms_per_step)
-    gemm_avg = sum(gemm_ms) / K
-    comb_avg = sum(comb_ms) / K
     peaks, peak_src = load_peaks()
-    alg_bytes = V * d * 2 + M * d * 2 + M * 12 + (M * V * 2 if surface == sb.SB_FULL_LOGITS else 0)
-    alg_flops = 2.0 * M * V * d
-    mem_bound = not args.workload.startswith("prefill")
-    achieved_gbs = alg_bytes / (gemm_avg * 1e-3) / 1e9
-    achieved_tfs = alg_flops / (gemm_avg * 1e-3) / 1e12
     tr = KERNEL_TRAFFIC.get(args.workload)
     traffic = tr["bytes"] if tr and tr.get("src_sha") == kernel_src_hash() else None
-    if mem_bound:
-        roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
-                "peak_source": f"{peak_src} (HBM copy, burst)", "kernel": "lmhead_kernel",
-                "kernel_ms": gemm_avg, "combine_ms": comb_avg,
-                "algorithmic_bytes": alg_bytes, "tensor_tflops": achieved_tfs,
-                "nominal": {"peak": NOMINAL_PEAKS["hbm_gbs"],
-                            "frac": achieved_gbs / NOMINAL_PEAKS["hbm_gbs"]}}
-    else:
-        roof = {"bound": "tensor", "achieved": achieved_tfs, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved_tfs / peaks["bf16_tflops"], "traffic": traffic,
-                "peak_source": f"{peak_src} (cuBLAS bf16, burst)", "kernel": "lmhead_kernel",
-                "kernel_ms": gemm_avg, "combine_ms": comb_avg, "algorithmic_flops": alg_flops,
-                "hbm_gbs": achieved_gbs,
-                "nominal": {"peak": NOMINAL_PEAKS["bf16_tflops"],
-                            "frac": achieved_tfs / NOMINAL_PEAKS["bf16_tflops"]}}
+    roof = projection_roofline(w, gemm_avg, comb_avg, peaks, peak_src,
+                               tensor_bound=args.workload.startswith("prefill"), traffic=traffic)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -568,6 +723,12 @@ def main():
         cpu = {"value": v, "unit": "rows/s", "cores": cores, "kind": "oracle",
                "sample": f"{n} rows in {el:.1f} s ({rows_per_call}-row calls against the full W)"}
 
+    per_cfg = None
+    if world == 1 and args.workload == "decode16" and args.per_config_seconds > 0:
+        del w, H, W, out, H_dev, H_host
+        torch.cuda.empty_cache()
+        per_cfg = per_config_table(args.per_config_seconds, peaks, peak_src, local)
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K,
@@ -578,7 +739,7 @@ def main():
                        "l2": ("inputs larger than L2 (W %.2f GB streamed every step)"
                               % (V * d * 2 / 1e9)) if flush is None else
                              ("inputs %.1f MB fit in L2: L2 flushed (2x L2 written) before "
-                              "every step, outside its events" % (in_bytes / 1e6)),
+                              "every step, outside its events" % (w_in_mb(V, d, M))),
                        "parallelism": "replicas" if world > 1 else "single"},
             "roofline": roof,
             "cpu_baseline": cpu,
@@ -591,10 +752,15 @@ def main():
             "clocks": clocks.summary(),
             "gpu_launches": 2 * K,
             "wall_s_timed": t_wall,
+            "per_config": per_cfg,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def w_in_mb(V, d, M):
+    return (V * d * 2 + M * d * 2) / 1e6
 
 
 if __name__ == "__main__":
