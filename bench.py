@@ -78,6 +78,8 @@ WORKLOADS = {
                                 desc="profiling case: H[16,1024] x W[151936,1024] bf16, k=4, top-8"),
     "sampling_token_mid": dict(M=256, d=5120, V=77824, k=4, surface="token_logprob",
                                desc="profiling case: H[256,5120] x W[77824,5120] bf16, k=4 (4 W tiles per CTA pair)"),
+    "sampling_mid": dict(M=256, d=5120, V=77824, k=4, surface="gumbel_token", T=0.7, seed=1234,
+                         desc="profiling case: H[256,5120] x W[77824,5120] bf16, k=4, GUMBEL (4 W tiles per CTA pair)"),
     "decode64_small": dict(M=64, d=1024, V=151936, k=2, surface="full_logits",
                            desc="profiling case: H[64,1024] x W[151936,1024] bf16, k=2, FULL_LOGITS"),
     "decode64_token_small": dict(M=64, d=1024, V=151936, k=2, surface="token_logprob",

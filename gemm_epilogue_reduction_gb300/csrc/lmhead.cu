@@ -283,9 +283,10 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
             uint32_t ok[cw], okm[cw];
 #pragma unroll
             for (int j = 0; j < cw; ++j) {
-                const float g = gumbel_from_bits(bits24_from_state(st));
+                // keys are compared less the constant -ln(ln 2), added back per record
+                const float kj = gumbel_key_less_c0(y[j], bits24_from_state(st));
                 st += static_cast<unsigned long long>(static_cast<unsigned>(p.V)) * kGolden;
-                ok[j] = float_to_ordered(valid ? y[j] + g : -INFINITY);
+                ok[j] = float_to_ordered(valid ? kj : -INFINITY);
             }
 #pragma unroll
             for (int j = 0; j < cw; ++j) okm[j] = __reduce_max_sync(0xFFFFFFFFu, ok[j]);
@@ -361,7 +362,7 @@ __device__ __forceinline__ void epilogue_vocab(const GemmParams &p, const TileCo
                     gz = sc_gz[w * nb + row];
                 }
             }
-            p.ws.gk[ri] = gk;
+            p.ws.gk[ri] = gk + kGumbelC0;
             p.ws.gi[ri] = gi;
             p.ws.gz[ri] = gz;
         }
@@ -541,10 +542,11 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
             unsigned long long st = splitmix_state(
                 p.seed, static_cast<unsigned long long>(row) * static_cast<unsigned>(p.V) +
                             static_cast<unsigned>(cb));
-            // columns past the shard end have y = -inf, so their key is -inf and never wins
+            // columns past the shard end have y = -inf, so their key is -inf and never wins;
+            // keys are compared less the constant -ln(ln 2), added back per record
 #pragma unroll
             for (int j = 0; j < 32; ++j, st += kGolden) {
-                const float key = y[j] + gumbel_from_bits(bits24_from_state(st));
+                const float key = gumbel_key_less_c0(y[j], bits24_from_state(st));
                 if (key > gk) {
                     gk = key;
                     gi = cb + j;
@@ -608,7 +610,7 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
         p.ws.idx[o] = ri;
         p.ws.s[o] = rs;
         if (GUMBEL) {
-            p.ws.gk[o] = gk;
+            p.ws.gk[o] = gk + kGumbelC0;
             p.ws.gi[o] = gi;
             p.ws.gz[o] = gz;
         }
