@@ -101,8 +101,8 @@ NOMINAL_PEAKS = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0}
 # null once the source differs.
 KERNEL_TRAFFIC = {
     # decode16: dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
-    # (1,556,127,488 + 3,217,152 B; W + H are 1,555,988,480 B).
-    "decode16": {"bytes": 1559344640, "src_sha": "e00d73faa972287d"},
+    # (1,556,172,288 + 2,995,456 B; W + H are 1,555,988,480 B).
+    "decode16": {"bytes": 1559167744, "src_sha": "82219ec0228f5a3d"},
 }
 
 
@@ -537,22 +537,27 @@ def measure_plan_costs(seconds, peaks, peak_src, gpu_index, ref="decode64",
     return sel, er, es
 
 
-PER_CONFIG = ("decode64", "decode64_token", "prefill", "sampling")
+PER_CONFIG = ("decode64", "decode64_token", "sampling", "prefill")
+IDLE_BETWEEN_S = 0.5  # the GPU idles this long before each entry (power state of the last)
 
 
 def per_config_table(seconds, peaks, peak_src, gpu_index):
-    """The other configurations, each timed on its own for about `seconds`, plus the partial
-    completion and the Equation (7) decision on the measured decode64 costs."""
+    """The other configurations, each timed on its own for about `seconds` after a short idle
+    gap (the power-capped prefill last, so it does not set the clocks of the others), plus
+    the partial completion and the Equation (7) decision on the measured decode64 costs."""
     out = {}
+    time.sleep(IDLE_BETWEEN_S)
     sel, out["decode64"], out["decode64_token"] = measure_plan_costs(seconds, peaks, peak_src,
                                                                      gpu_index)
-    for name in PER_CONFIG[2:]:
-        out[name] = measure_workload(name, seconds, peaks, peak_src, gpu_index)
+    time.sleep(IDLE_BETWEEN_S)
     ms, n, roof, clk, _, _ = measure_partial("mlp_down", seconds, peaks, peak_src, gpu_index)
     out["mlp_down"] = {"desc": WORKLOADS["mlp_down"]["desc"], "steps": n, "step_us": ms * 1e3,
                        "rows_per_s": WORKLOADS["mlp_down"]["M"] / (ms * 1e-3),
                        "bound": "hbm", "frac": roof["frac"], "achieved": roof["achieved"],
                        "unit": "GB/s", "nominal_frac": roof["nominal"]["frac"], "clocks": clk}
+    for name in PER_CONFIG[2:]:
+        time.sleep(IDLE_BETWEEN_S)
+        out[name] = measure_workload(name, seconds, peaks, peak_src, gpu_index)
     out["selection"] = sel
     return out
 
