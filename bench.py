@@ -692,7 +692,7 @@ def main():
         stream.synchronize()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / E
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / E, "cuda")
     e2e_h2d = M * d * 2
     e2e_d2h = 2 * M * 4
 
@@ -709,7 +709,7 @@ def main():
         stream.synchronize()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_graph_ms = e0.elapsed_time(e1) / E
+    e2e_graph_ms = max_over_ranks(e0.elapsed_time(e1) / E, "cuda")
     hstep.close()
 
     ms_per_step = total_ms / K
