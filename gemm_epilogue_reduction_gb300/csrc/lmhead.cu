@@ -11,9 +11,11 @@
 // Structure (the warp roles and TMEM epilogue of the "01 · 通算融合" note on Blackwell
 // SM100 GEMMs, sections 2 and 5.1: TMA producer, MMA issuer, epilogue warps; full-K
 // accumulation before any epilogue work):
-//   warps 0, 2  one lane each issues TMA loads of 64-wide K slices of one operand into its
-//               own ring of shared-memory stages (128-byte swizzle); the ring of the
-//               operand streamed from HBM (W) is deeper than the one re-read from L2 (H);
+//   warps 0, 2  TMA producers (one lane each) of 64-wide K slices (128-byte swizzle).
+//               Vocab mode: one ring per operand, the ring of the operand streamed from HBM
+//               (W) deeper than the one re-read from L2 (H).  Rows mode: warp 0 alone fills
+//               one ring of joint stages (H rows and this CTA's half of the W tile), so the
+//               MMA waits on one barrier and commits once per K block;
 //   warp 1      owns the TMEM allocation; one lane issues tcgen05.mma (M = 128, or
 //               M = 256 over a CTA pair in rows mode; bf16 x bf16 -> fp32) into one of two
 //               TMEM accumulators and commits stage releases and "accumulator full" to
@@ -626,26 +628,18 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
 }
 
 // ------------------------------------------------------------------ the kernel
-// One producer per operand ring, so the operand streamed from HBM (W) can run further ahead
-// of the MMA than the one re-read from L2 (H).
-template <int NSTAGES_MAX>
+// Vocab mode: one producer per operand ring, so the operand streamed from HBM (W) can run
+// further ahead of the MMA than the one re-read from L2 (H).
 __device__ __forceinline__ void produce_ring(const GemmParams &p, const CUtensorMap *tm,
                                              uint8_t *ring, uint32_t stage_bytes, int stages,
                                              uint64_t *full, uint64_t *empty, bool is_a,
-                                             int rank, uint64_t policy, int unit0,
-                                             int unit_stride, volatile int *abort_flag,
-                                             TileCoord (*coord)(const GemmParams &, int, int),
-                                             bool pair, uint32_t pre) {
-    // pair: the leader's barrier counts both CTAs' bytes; the peer's copies complete on the
-    // leader's barrier (at the same offset), and the peer's empty barriers are armed by the
-    // leader's MMA commits (cluster-scope acquire)
-    const bool peer = pair && rank == 1;
-    const bool leader = pair && rank == 0;
+                                             uint64_t policy, int unit0, int unit_stride,
+                                             volatile int *abort_flag, uint32_t pre) {
     int stage = 0;
     uint32_t phase = 0, issued = 0;
     bool ok = true;
     for (int tile = unit0; ok && tile < p.num_tiles; tile += unit_stride) {
-        const TileCoord c = coord(p, tile, rank);
+        const TileCoord c = tile_coord<true>(p, tile, 0);
         const int row = is_a ? c.a_row : c.b_row;
         for (int kb = 0; kb < p.kblocks; ++kb) {
             if (issued < pre) {  // already issued before the wait on the previous kernel
@@ -656,17 +650,12 @@ __device__ __forceinline__ void produce_ring(const GemmParams &p, const CUtensor
                 }
                 continue;
             }
-            if (!(pair ? bwait_cl(&empty[stage], phase ^ 1u, abort_flag, p)
-                       : bwait(&empty[stage], phase ^ 1u, abort_flag, p))) {
+            if (!bwait(&empty[stage], phase ^ 1u, abort_flag, p)) {
                 ok = false;
                 break;
             }
-            if (!peer) mbar_arrive_expect_tx(&full[stage], leader ? 2 * stage_bytes : stage_bytes);
-            uint8_t *dst = ring + stage * stage_bytes;
-            if (peer)
-                tma_load_2d_pair(dst, tm, mapa_rank(&full[stage], 0), kb * kBlockK, row, policy);
-            else
-                tma_load_2d(dst, tm, &full[stage], kb * kBlockK, row, policy);
+            mbar_arrive_expect_tx(&full[stage], stage_bytes);
+            tma_load_2d(ring + stage * stage_bytes, tm, &full[stage], kb * kBlockK, row, policy);
             ++issued;
             if (++stage == stages) {
                 stage = 0;
@@ -676,6 +665,57 @@ __device__ __forceinline__ void produce_ring(const GemmParams &p, const CUtensor
     }
     // Drain: the last `stages` issues may still be landing (only possible after an abort;
     // on the normal path the MMA warp consumed every one of them).
+    const uint32_t n = issued < static_cast<uint32_t>(stages) ? issued : stages;
+    for (uint32_t i = issued - n; i < issued; ++i)
+        if (!bwait_drain(&full[i % stages], (i / stages) & 1u, abort_flag, p)) break;
+}
+
+// Rows mode (CTA pairs): one ring of joint stages, each holding this CTA's 128 H rows (A,
+// 16 KB) and its half of the W tile (B, 16 KB) for one K block; one thread per CTA loads
+// both.  The leader's full barrier counts the four copies of the pair; the peer's copies
+// complete on it (at the same offset), and the leader's single MMA commit per stage frees
+// the stage in both CTAs (the peer waits on its own empty barrier with cluster-scope
+// acquire).  The first `pre` stages' W copies (and the leader's expect) went out before the
+// wait on the previous kernel; their H copies go out here.
+__device__ __forceinline__ void produce_pair(const GemmParams &p, const CUtensorMap *tmA,
+                                             const CUtensorMap *tmB, uint8_t *sA, uint8_t *sB,
+                                             uint32_t b_bytes, uint64_t *full, uint64_t *empty,
+                                             int rank, int unit0, int unit_stride,
+                                             volatile int *abort_flag, uint32_t pre) {
+    const bool peer = rank == 1;
+    const int stages = p.stages_a;
+    const uint64_t pol_a = policy_evict_last(), pol_b = policy_evict_normal();
+    int stage = 0;
+    uint32_t phase = 0, issued = 0;
+    bool ok = true;
+    for (int tile = unit0; ok && tile < p.num_tiles; tile += unit_stride) {
+        const TileCoord c = tile_coord<false>(p, tile, rank);
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+            const bool w_done = issued < pre;
+            if (!w_done) {
+                if (!bwait_cl(&empty[stage], phase ^ 1u, abort_flag, p)) {
+                    ok = false;
+                    break;
+                }
+                if (!peer) mbar_arrive_expect_tx(&full[stage], 2 * (kStageBytesA + b_bytes));
+            }
+            uint8_t *da = sA + stage * kStageBytesA;
+            uint8_t *db = sB + stage * b_bytes;
+            if (peer) {
+                const uint32_t fb = mapa_rank(&full[stage], 0);
+                tma_load_2d_pair(da, tmA, fb, kb * kBlockK, c.a_row, pol_a);
+                if (!w_done) tma_load_2d_pair(db, tmB, fb, kb * kBlockK, c.b_row, pol_b);
+            } else {
+                tma_load_2d(da, tmA, &full[stage], kb * kBlockK, c.a_row, pol_a);
+                if (!w_done) tma_load_2d(db, tmB, &full[stage], kb * kBlockK, c.b_row, pol_b);
+            }
+            ++issued;
+            if (++stage == stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
     if (peer) {
         // the peer cannot observe its copies (they complete on the leader's barrier); after
         // an abort it gives the last ones a bounded time to land (they were issued at least
@@ -687,16 +727,11 @@ __device__ __forceinline__ void produce_ring(const GemmParams &p, const CUtensor
         }
         return;
     }
-    // A pair leader's barrier also waits for the peer's bytes, which never come for a stage
-    // the peer did not issue: the drain stops at the first wait that runs out.
+    // The leader's barrier also waits for the peer's bytes, which never come for a stage the
+    // peer did not issue: the drain stops at the first wait that runs out.
     const uint32_t n = issued < static_cast<uint32_t>(stages) ? issued : stages;
     for (uint32_t i = issued - n; i < issued; ++i)
         if (!bwait_drain(&full[i % stages], (i / stages) & 1u, abort_flag, p)) break;
-}
-
-template <bool VOCAB>
-__device__ TileCoord coord_fn(const GemmParams &p, int tile, int rank) {
-    return tile_coord<VOCAB>(p, tile, rank);
 }
 
 template <bool VOCAB, int EPI>
@@ -788,20 +823,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         c.a_row, pol);
         }
     }
-    // Rows mode with CTA pairs: the same for W, operand B, in both CTAs of the pair (the
-    // peer's copies complete on the leader's barriers, as in the ring loop below).
+    // Rows mode with CTA pairs: the same for W, operand B, in both CTAs of the pair, into the
+    // joint stages (the leader expects the whole stage, H included, which its producer loads
+    // after the wait; the peer's copies complete on the leader's barriers).
     uint32_t b_pre = 0;
-    if (PAIR && warp == 2 && lane == 0 && unit0 < p.num_tiles) {
-        b_pre = static_cast<uint32_t>(p.stages_b < p.kblocks ? p.stages_b : p.kblocks);
+    if (PAIR && warp == 0 && lane == 0 && unit0 < p.num_tiles) {
+        b_pre = static_cast<uint32_t>(p.stages_a < p.kblocks ? p.stages_a : p.kblocks);
         const TileCoord c = tile_coord<VOCAB>(p, unit0, rank);
         const uint64_t pol = policy_evict_normal();
         for (uint32_t kb = 0; kb < b_pre; ++kb) {
             uint8_t *dst = sB + kb * b_stage_bytes;
             if (rank == 0) {
-                mbar_arrive_expect_tx(&fullB[kb], 2 * b_stage_bytes);
-                tma_load_2d(dst, &tmB, &fullB[kb], static_cast<int>(kb) * kBlockK, c.b_row, pol);
+                mbar_arrive_expect_tx(&fullA[kb], 2 * (kStageBytesA + b_stage_bytes));
+                tma_load_2d(dst, &tmB, &fullA[kb], static_cast<int>(kb) * kBlockK, c.b_row, pol);
             } else {
-                tma_load_2d_pair(dst, &tmB, mapa_rank(&fullB[kb], 0),
+                tma_load_2d_pair(dst, &tmB, mapa_rank(&fullA[kb], 0),
                                  static_cast<int>(kb) * kBlockK, c.b_row, pol);
             }
         }
@@ -826,22 +862,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0 || warp == 2) {
-        // ------------------------------------------------ TMA producers (one lane each):
-        // warp 0 fills ring A, warp 2 ring B.  W is streamed once (evict first in vocab
-        // mode); H and shared W tiles are re-read from L2.
+        // ------------------------------------------------ TMA producers (one lane each).
+        // Vocab mode: warp 0 fills ring A (W, streamed once, evict first), warp 2 ring B (H,
+        // re-read from L2).  Rows mode: warp 0 fills the joint stages (H and the CTA's half
+        // of the W tile); warp 2 has no work.
         if (lane == 0) {
-            if (warp == 0)
-                produce_ring<kMaxStages>(p, &tmA, sA, kStageBytesA, p.stages_a, fullA, emptyA,
-                                         true, rank,
-                                         VOCAB ? policy_evict_first() : policy_evict_last(),
-                                         unit0, unit_stride, abort_flag, coord_fn<VOCAB>, PAIR,
-                                         a_pre);
-            else
-                produce_ring<kMaxStages>(p, &tmB, sB, b_stage_bytes, p.stages_b, fullB, emptyB,
-                                         false, rank,
-                                         VOCAB ? policy_evict_last() : policy_evict_normal(),
-                                         unit0, unit_stride, abort_flag, coord_fn<VOCAB>, PAIR,
-                                         b_pre);
+            if (!VOCAB) {
+                if (warp == 0)
+                    produce_pair(p, &tmA, &tmB, sA, sB, b_stage_bytes, fullA, emptyA, rank,
+                                 unit0, unit_stride, abort_flag, b_pre);
+            } else if (warp == 0) {
+                produce_ring(p, &tmA, sA, kStageBytesA, p.stages_a, fullA, emptyA, true,
+                             policy_evict_first(), unit0, unit_stride, abort_flag, a_pre);
+            } else {
+                produce_ring(p, &tmB, sB, b_stage_bytes, p.stages_b, fullB, emptyB, false,
+                             policy_evict_last(), unit0, unit_stride, abort_flag, 0);
+            }
         }
     } else if (warp == 1) {
         if (PAIR && rank == 1) {
@@ -852,8 +888,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 const uint32_t idesc = idesc_bf16_f32(2 * kTileA, p.nb);
                 constexpr uint16_t kBoth = 3;
-                int sa = 0, sb = 0;
-                uint32_t pa = 0, pb = 0;
+                int st = 0;
+                uint32_t ph = 0;
                 bool ok = true, any = false;
                 int it = 0;
                 for (int tile = unit0; ok && tile < p.num_tiles; tile += unit_stride, ++it) {
@@ -863,29 +899,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * p.nb);
                     for (int kb = 0; kb < p.kblocks; ++kb) {
-                        // the leader's barriers count both CTAs' bytes
-                        if (!bwait(&fullA[sa], pa, abort_flag, p) ||
-                            !bwait(&fullB[sb], pb, abort_flag, p)) {
+                        // the leader's barrier counts the whole joint stage of both CTAs
+                        if (!bwait(&fullA[st], ph, abort_flag, p)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + sa * kStageBytesA));
-                        const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + sb * b_stage_bytes));
+                        const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + st * kStageBytesA));
+                        const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + st * b_stage_bytes));
 #pragma unroll
                         for (int ks = 0; ks < kBlockK / 16; ++ks)
                             umma_bf16_pair(d_tmem, adesc + 2u * ks, bdesc + 2u * ks, idesc,
                                            (kb | ks) != 0 ? 1u : 0u);
-                        umma_commit_pair(&emptyA[sa], kBoth);  // frees the stage in both CTAs
-                        umma_commit_pair(&emptyB[sb], kBoth);
+                        // one commit per stage (each commit costs the tensor pipe time):
+                        // frees the joint stage in both CTAs
+                        umma_commit_pair(&emptyA[st], kBoth);
                         any = true;
-                        if (++sa == p.stages_a) {
-                            sa = 0;
-                            pa ^= 1u;
-                        }
-                        if (++sb == p.stages_b) {
-                            sb = 0;
-                            pb ^= 1u;
+                        if (++st == p.stages_a) {
+                            st = 0;
+                            ph ^= 1u;
                         }
                     }
                     if (ok) umma_commit_pair(&tfull[b], kBoth);

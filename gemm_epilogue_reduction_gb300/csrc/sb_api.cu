@@ -196,22 +196,22 @@ int32_t check_outputs(const sb_outputs *out, int32_t surface, bool need_ws) {
 #ifndef SB_VOCAB_STAGES_B
 #define SB_VOCAB_STAGES_B 4
 #endif
-#ifndef SB_ROWS_STAGES_A
-#define SB_ROWS_STAGES_A 4
-#endif
-
-// Ring depths: the ring of the operand re-read from L2 (H) gets a fixed depth, the ring of
-// the operand streamed from HBM (W) every remaining stage that fits in shared memory.
+// Ring depths.  Vocab mode: the ring of the operand re-read from L2 (H) gets a fixed depth,
+// the ring of the operand streamed from HBM (W) every remaining stage that fits in shared
+// memory.  Rows mode: joint stages (this CTA's H rows and its half of the W tile for one K
+// block), as many as fit.
 bool pick_stages(int nb, bool vm, int m_tiles, int flags, int topk, int *sa, int *sb) {
     (void)m_tiles;
     if (vm) {  // A = W (streamed), B = H
         *sb = SB_VOCAB_STAGES_B;
         for (*sa = kMaxStages; *sa > 1; --*sa)
             if (lmhead_smem_bytes(nb, *sa, *sb, vm, flags, topk) <= kSmemLimit) break;
-    } else {   // A = H, B = W tile (streamed or shared by the cluster)
-        *sa = SB_ROWS_STAGES_A;
-        for (*sb = kMaxStages; *sb > 1; --*sb)
+    } else {   // A = H, B = W half-tile, one joint ring
+        for (*sa = kMaxStages; *sa > 1; --*sa) {
+            *sb = *sa;
             if (lmhead_smem_bytes(nb, *sa, *sb, vm, flags, topk) <= kSmemLimit) break;
+        }
+        *sb = *sa;
     }
     return lmhead_smem_bytes(nb, *sa, *sb, vm, flags, topk) <= kSmemLimit && *sa >= 2 && *sb >= 2;
 }
