@@ -61,14 +61,14 @@ struct SmemLayout {
 // Shared memory: ring A (stages_a x 16 KB), ring B (stages_b x nb*128 B), mbarriers,
 // TMEM address + abort flag, vocab-mode target ids and cross-quadrant scratch.
 __host__ __device__ inline SmemLayout make_layout(int nb, int stages_a, int stages_b, bool vocab,
-                                                  int flags, int topk) {
+                                                  int flags, int topk, int atoms) {
     SmemLayout L;
     uint32_t off = 0;
     L.a_off = off;
-    off += stages_a * kStageBytesA;
+    off += stages_a * kStageBytesA * (vocab ? 1 : atoms);
     L.b_off = off;
     // rows mode (CTA pairs): each CTA stages only its half of the W tile
-    off += stages_b * (vocab ? nb : nb / 2) * 128;
+    off += stages_b * (vocab ? nb : nb / 2) * 128 * (vocab ? 1 : atoms);
     L.bar_off = off;
     off += (4 * kMaxStages + 8) * 8;
     L.misc_off = off;
@@ -670,20 +670,22 @@ __device__ __forceinline__ void produce_ring(const GemmParams &p, const CUtensor
         if (!bwait_drain(&full[i % stages], (i / stages) & 1u, abort_flag, p)) break;
 }
 
-// Rows mode (CTA pairs): one ring of joint stages, each holding this CTA's 128 H rows (A,
-// 16 KB) and its half of the W tile (B, 16 KB) for one K block; one thread per CTA loads
-// both.  The leader's full barrier counts the four copies of the pair; the peer's copies
-// complete on it (at the same offset), and the leader's single MMA commit per stage frees
-// the stage in both CTAs (the peer waits on its own empty barrier with cluster-scope
-// acquire).  The first `pre` stages' W copies (and the leader's expect) went out before the
-// wait on the previous kernel; their H copies go out here.
+// Rows mode (CTA pairs): one ring of joint stages, each holding this CTA's 128 H rows (A)
+// and its half of the W tile (B) for one K block of ATOMS 64-wide atoms (16 KB per atom and
+// operand); one thread per CTA loads both.  The leader's full barrier counts every
+// copy of the pair; the peer's copies complete on it (at the same offset), and the leader's
+// single MMA commit per stage frees the stage in both CTAs (the peer waits on its own empty
+// barrier with cluster-scope acquire).  The first `pre` stages' W copies (and the leader's
+// expect) went out before the wait on the previous kernel; their H copies go out here.
+template <int ATOMS>
 __device__ __forceinline__ void produce_pair(const GemmParams &p, const CUtensorMap *tmA,
                                              const CUtensorMap *tmB, uint8_t *sA, uint8_t *sB,
-                                             uint32_t b_bytes, uint64_t *full, uint64_t *empty,
+                                             uint32_t b_atom, uint64_t *full, uint64_t *empty,
                                              int rank, int unit0, int unit_stride,
                                              volatile int *abort_flag, uint32_t pre) {
     const bool peer = rank == 1;
     const int stages = p.stages_a;
+    const uint32_t a_stage = kStageBytesA * ATOMS, b_stage = b_atom * ATOMS;
     const uint64_t pol_a = policy_evict_last(), pol_b = policy_evict_normal();
     int stage = 0;
     uint32_t phase = 0, issued = 0;
@@ -697,17 +699,21 @@ __device__ __forceinline__ void produce_pair(const GemmParams &p, const CUtensor
                     ok = false;
                     break;
                 }
-                if (!peer) mbar_arrive_expect_tx(&full[stage], 2 * (kStageBytesA + b_bytes));
+                if (!peer) mbar_arrive_expect_tx(&full[stage], 2 * (a_stage + b_stage));
             }
-            uint8_t *da = sA + stage * kStageBytesA;
-            uint8_t *db = sB + stage * b_bytes;
-            if (peer) {
-                const uint32_t fb = mapa_rank(&full[stage], 0);
-                tma_load_2d_pair(da, tmA, fb, kb * kBlockK, c.a_row, pol_a);
-                if (!w_done) tma_load_2d_pair(db, tmB, fb, kb * kBlockK, c.b_row, pol_b);
-            } else {
-                tma_load_2d(da, tmA, &full[stage], kb * kBlockK, c.a_row, pol_a);
-                if (!w_done) tma_load_2d(db, tmB, &full[stage], kb * kBlockK, c.b_row, pol_b);
+            uint8_t *da = sA + stage * a_stage;
+            uint8_t *db = sB + stage * b_stage;
+            const uint32_t fb = peer ? mapa_rank(&full[stage], 0) : 0u;
+#pragma unroll
+            for (int at = 0; at < ATOMS; ++at) {
+                const int k0 = (kb * ATOMS + at) * kBlockK;  // past d: read as zeros
+                if (peer) {
+                    tma_load_2d_pair(da + at * kStageBytesA, tmA, fb, k0, c.a_row, pol_a);
+                    if (!w_done) tma_load_2d_pair(db + at * b_atom, tmB, fb, k0, c.b_row, pol_b);
+                } else {
+                    tma_load_2d(da + at * kStageBytesA, tmA, &full[stage], k0, c.a_row, pol_a);
+                    if (!w_done) tma_load_2d(db + at * b_atom, tmB, &full[stage], k0, c.b_row, pol_b);
+                }
             }
             ++issued;
             if (++stage == stages) {
@@ -734,14 +740,15 @@ __device__ __forceinline__ void produce_pair(const GemmParams &p, const CUtensor
         if (!bwait_drain(&full[i % stages], (i / stages) & 1u, abort_flag, p)) break;
 }
 
-template <bool VOCAB, int EPI>
+template <bool VOCAB, int EPI, int ATOMS>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const GemmParams p, const uint32_t tmem_cols) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    const SmemLayout L = make_layout(p.nb, p.stages_a, p.stages_b, VOCAB, p.flags, p.topk);
+    const SmemLayout L = make_layout(p.nb, p.stages_a, p.stages_b, VOCAB, p.flags, p.topk,
+                                     ATOMS);
     uint8_t *sA = smem + L.a_off;
     uint8_t *sB = smem + L.b_off;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
@@ -766,6 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // peer's copies complete on the leader's stage barriers, which count both CTAs' bytes.
     constexpr int CS = VOCAB ? 1 : kRowsCluster;
     constexpr bool PAIR = !VOCAB;
+    // B bytes per 64-wide K atom (vocab mode: one atom per stage; rows mode: ATOMS)
     const uint32_t b_stage_bytes = static_cast<uint32_t>(PAIR ? p.nb / 2 : p.nb) * 128u;
     // CTAs of a cluster walk the same work units in lockstep (same ring positions).
     const int rank = CS > 1 ? static_cast<int>(cluster_ctarank()) : 0;
@@ -832,13 +840,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const TileCoord c = tile_coord<VOCAB>(p, unit0, rank);
         const uint64_t pol = policy_evict_normal();
         for (uint32_t kb = 0; kb < b_pre; ++kb) {
-            uint8_t *dst = sB + kb * b_stage_bytes;
-            if (rank == 0) {
-                mbar_arrive_expect_tx(&fullA[kb], 2 * (kStageBytesA + b_stage_bytes));
-                tma_load_2d(dst, &tmB, &fullA[kb], static_cast<int>(kb) * kBlockK, c.b_row, pol);
-            } else {
-                tma_load_2d_pair(dst, &tmB, mapa_rank(&fullA[kb], 0),
-                                 static_cast<int>(kb) * kBlockK, c.b_row, pol);
+            uint8_t *dst = sB + kb * b_stage_bytes * ATOMS;
+            if (rank == 0)
+                mbar_arrive_expect_tx(&fullA[kb], 2 * ATOMS * (kStageBytesA + b_stage_bytes));
+#pragma unroll
+            for (int at = 0; at < ATOMS; ++at) {
+                const int k0 = (static_cast<int>(kb) * ATOMS + at) * kBlockK;
+                if (rank == 0)
+                    tma_load_2d(dst + at * b_stage_bytes, &tmB, &fullA[kb], k0, c.b_row, pol);
+                else
+                    tma_load_2d_pair(dst + at * b_stage_bytes, &tmB, mapa_rank(&fullA[kb], 0),
+                                     k0, c.b_row, pol);
             }
         }
     }
@@ -869,7 +881,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             if (!VOCAB) {
                 if (warp == 0)
-                    produce_pair(p, &tmA, &tmB, sA, sB, b_stage_bytes, fullA, emptyA, rank,
+                    produce_pair<ATOMS>(p, &tmA, &tmB, sA, sB, b_stage_bytes, fullA, emptyA, rank,
                                  unit0, unit_stride, abort_flag, b_pre);
             } else if (warp == 0) {
                 produce_ring(p, &tmA, sA, kStageBytesA, p.stages_a, fullA, emptyA, true,
@@ -888,8 +900,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 const uint32_t idesc = idesc_bf16_f32(2 * kTileA, p.nb);
                 constexpr uint16_t kBoth = 3;
+                // descriptors of stage 0; a stage / atom / 16-column step adds its byte offset
+                // >> 4 to the start-address field (shared memory stays below 256 KB, so the
+                // 14-bit field never carries)
+                const uint64_t adesc0 = sw128_kmajor_desc(smem_u32(sA));
+                const uint64_t bdesc0 = sw128_kmajor_desc(smem_u32(sB));
+                const uint32_t a_step = (kStageBytesA * ATOMS) >> 4;
+                const uint32_t b_step = (b_stage_bytes * ATOMS) >> 4;
                 int st = 0;
-                uint32_t ph = 0;
+                uint32_t ph = 0, a_off = 0, b_off = 0;
                 bool ok = true, any = false;
                 int it = 0;
                 for (int tile = unit0; ok && tile < p.num_tiles; tile += unit_stride, ++it) {
@@ -905,19 +924,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         tc_fence_after();
-                        const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + st * kStageBytesA));
-                        const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + st * b_stage_bytes));
 #pragma unroll
-                        for (int ks = 0; ks < kBlockK / 16; ++ks)
-                            umma_bf16_pair(d_tmem, adesc + 2u * ks, bdesc + 2u * ks, idesc,
-                                           (kb | ks) != 0 ? 1u : 0u);
+                        for (int at = 0; at < ATOMS; ++at) {
+                            const uint64_t adesc = adesc0 + a_off + at * (kStageBytesA >> 4);
+                            const uint64_t bdesc = bdesc0 + b_off + at * (b_stage_bytes >> 4);
+#pragma unroll
+                            for (int ks = 0; ks < kBlockK / 16; ++ks)
+                                umma_bf16_pair(d_tmem, adesc + 2u * ks, bdesc + 2u * ks, idesc,
+                                               (kb | at | ks) != 0 ? 1u : 0u);
+                        }
                         // one commit per stage (each commit costs the tensor pipe time):
                         // frees the joint stage in both CTAs
                         umma_commit_pair(&emptyA[st], kBoth);
                         any = true;
+                        a_off += a_step;
+                        b_off += b_step;
                         if (++st == p.stages_a) {
                             st = 0;
                             ph ^= 1u;
+                            a_off = 0;
+                            b_off = 0;
                         }
                     }
                     if (ok) umma_commit_pair(&tfull[b], kBoth);
@@ -1015,11 +1041,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool VOCAB, int EPI>
-cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p,
+template <bool VOCAB, int EPI, int ATOMS>
+cudaError_t launch_t1(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p,
                      size_t smem, int num_sms, cudaStream_t stream) {
     constexpr int CS = VOCAB ? 1 : kRowsCluster;
-    auto kern = lmhead_kernel<VOCAB, EPI>;
+    auto kern = lmhead_kernel<VOCAB, EPI, ATOMS>;
     // The shared-memory opt-in is per device; every launch asks for at most kSmemLimit.
     static std::atomic<uint64_t> opted_in{0};
     int dev = 0;
@@ -1076,11 +1102,22 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmP
     return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p, cols);
 }
 
+// Rows mode: the kernel specialised for the call's atoms per joint stage (1 or 2).
+template <bool VOCAB, int EPI>
+cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p,
+                     size_t smem, int num_sms, cudaStream_t stream) {
+    if constexpr (!VOCAB) {
+        if (p.atoms == kMaxPairAtoms)
+            return launch_t1<false, EPI, kMaxPairAtoms>(tmA, tmB, p, smem, num_sms, stream);
+    }
+    return launch_t1<VOCAB, EPI, 1>(tmA, tmB, p, smem, num_sms, stream);
+}
+
 }  // namespace
 
 size_t lmhead_smem_bytes(int nb, int stages_a, int stages_b, bool vocab_mode, int flags,
-                         int topk) {
-    return make_layout(nb, stages_a, stages_b, vocab_mode, flags, topk).total;
+                         int topk, int atoms) {
+    return make_layout(nb, stages_a, stages_b, vocab_mode, flags, topk, atoms).total;
 }
 
 cudaError_t launch_lmhead(bool vocab_mode, const CUtensorMap &tmA, const CUtensorMap &tmB,

@@ -199,21 +199,21 @@ int32_t check_outputs(const sb_outputs *out, int32_t surface, bool need_ws) {
 // Ring depths.  Vocab mode: the ring of the operand re-read from L2 (H) gets a fixed depth,
 // the ring of the operand streamed from HBM (W) every remaining stage that fits in shared
 // memory.  Rows mode: joint stages (this CTA's H rows and its half of the W tile for one K
-// block), as many as fit.
-bool pick_stages(int nb, bool vm, int m_tiles, int flags, int topk, int *sa, int *sb) {
-    (void)m_tiles;
+// block of `atoms` 64-wide slices), as many as fit.
+bool pick_stages(int nb, bool vm, int atoms, int flags, int topk, int *sa, int *sb) {
     if (vm) {  // A = W (streamed), B = H
         *sb = SB_VOCAB_STAGES_B;
         for (*sa = kMaxStages; *sa > 1; --*sa)
-            if (lmhead_smem_bytes(nb, *sa, *sb, vm, flags, topk) <= kSmemLimit) break;
+            if (lmhead_smem_bytes(nb, *sa, *sb, vm, flags, topk, 1) <= kSmemLimit) break;
     } else {   // A = H, B = W half-tile, one joint ring
         for (*sa = kMaxStages; *sa > 1; --*sa) {
             *sb = *sa;
-            if (lmhead_smem_bytes(nb, *sa, *sb, vm, flags, topk) <= kSmemLimit) break;
+            if (lmhead_smem_bytes(nb, *sa, *sb, vm, flags, topk, atoms) <= kSmemLimit) break;
         }
         *sb = *sa;
     }
-    return lmhead_smem_bytes(nb, *sa, *sb, vm, flags, topk) <= kSmemLimit && *sa >= 2 && *sb >= 2;
+    return lmhead_smem_bytes(nb, *sa, *sb, vm, flags, topk, vm ? 1 : atoms) <= kSmemLimit &&
+           *sa >= 2 && *sb >= 2;
 }
 
 CombineParams combine_params(const sb_outputs *out, const Workspace &w, int64_t M, int32_t k,
@@ -337,8 +337,14 @@ int32_t prepare(const void *H, const void *W, int64_t M, int64_t d, int64_t V, i
     const int64_t tiles = static_cast<int64_t>(k) * p.Tt * p.m_groups;
     if (tiles >= (int64_t(1) << 31)) return SB_ERR_INVALID_ARG;
     p.num_tiles = static_cast<int>(tiles);
-    p.kblocks = static_cast<int>((d + kBlockK - 1) / kBlockK);
-    if (!pick_stages(p.nb, vm, p.m_tiles, flags, K, &p.stages_a, &p.stages_b))
+    // K blocks: 64 columns in vocab mode.  Rows mode: K blocks of two 64-wide atoms (half the
+    // barrier waits and MMA commits per flop, 3 joint stages) when the rows span several CTA
+    // pairs, so that each W tile is shared by several pairs and the tensor pipe sets the pace;
+    // one atom (7 joint stages, deeper buffering of the W stream) for a single pair of M tiles.
+    p.atoms = (vm || p.m_groups < 2) ? 1 : kMaxPairAtoms;
+    const int64_t kb_cols = static_cast<int64_t>(p.atoms) * kBlockK;
+    p.kblocks = static_cast<int>((d + kb_cols - 1) / kb_cols);
+    if (!pick_stages(p.nb, vm, p.atoms, flags, K, &p.stages_a, &p.stages_b))
         return SB_ERR_UNSUPPORTED;
     p.flags = flags;
     p.topk = K;
@@ -355,7 +361,7 @@ int32_t prepare(const void *H, const void *W, int64_t M, int64_t d, int64_t V, i
                        : (make_map(&pr->tmA, H, M, d, kTileA) &&
                           make_map(&pr->tmB, W, V, d, kRowsTileN / p.cluster));
     if (!ok) return SB_ERR_CUDA;
-    pr->smem = lmhead_smem_bytes(p.nb, p.stages_a, p.stages_b, vm, flags, K);
+    pr->smem = lmhead_smem_bytes(p.nb, p.stages_a, p.stages_b, vm, flags, K, p.atoms);
     pr->sms = dev.sms;
     pr->vm = vm;
     pr->c = combine_params(out, p.ws, M, k, T, flags, inv_t);

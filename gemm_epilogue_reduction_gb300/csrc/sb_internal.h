@@ -21,6 +21,10 @@ constexpr int kMaxShards = 1024;  // largest k (the combine keeps k shard record
 // rows mode: a cluster of two CTAs (consecutive M tiles) shares each W tile; one
 // cta_group::2 MMA per pair, each CTA staging its own half of the W tile
 constexpr int kRowsCluster = 2;
+// rows mode: each joint pipeline stage holds 1 or kMaxPairAtoms 64-wide K slices ("atoms")
+// of both operands; with 2 (K block 128) the MMA warp waits once and commits once per
+// 8 MMAs, with 1 more stages fit in shared memory
+constexpr int kMaxPairAtoms = 2;
 
 constexpr int kEpiWarps = 8;         // two epilogue warps per TMEM lane quadrant
 constexpr int kFirstEpiWarp = 3;     // warps 0 and 2 load, warp 1 issues MMAs + owns TMEM
@@ -64,6 +68,7 @@ struct GemmParams {
     int kblocks;
     int stages_a;          // ring depth of the UMMA A operand (16 KB stages)
     int stages_b;          // ring depth of the UMMA B operand (nb * 128 B stages)
+    int atoms;             // rows mode: 64-wide K atoms per joint stage (1 or 2)
     int flags;
     int topk;              // K of the top-K surface (0 otherwise)
     float inv_t;
@@ -108,7 +113,7 @@ cudaError_t launch_copy16(void *dst, const void *src, size_t n16, int num_sms,
                           cudaStream_t stream);
 
 size_t lmhead_smem_bytes(int nb, int stages_a, int stages_b, bool vocab_mode, int flags,
-                         int topk);
+                         int topk, int atoms);
 
 // Host helpers shared by the entry points (sb_api.cu).
 bool encode_bf16_map(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols,
