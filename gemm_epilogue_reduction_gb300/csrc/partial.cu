@@ -20,11 +20,12 @@
 // Y: it sums the tile's slabs in ascending K order -- lane 0's first -- and writes Y.  The
 // summation order is fixed, so the result bits never depend on scheduling.
 //
-// partial_kernel: persistent, 224 threads.  Warp 0 issues TMA loads of W (128 rows, the
-// UMMA A operand) into the W ring, warp 6 loads of X (all M rows, the B operand) into the X
-// ring; warp 1 owns TMEM (two accumulators) and issues tcgen05.mma; warps 2-5 read the
-// accumulator (warp w reads TMEM lanes 32*(w%4)..) and store the slab.  All waits are
-// time-bounded (sb_pipe.cuh).
+// partial_kernel: persistent, 192 threads.  Warp 0 issues the TMA loads of one ring of
+// joint stages, each holding one K block of W (128 rows, the UMMA A operand) and of X (all M
+// rows, the B operand), so the MMA warp waits once and commits once per K block; warp 1 owns
+// TMEM (two accumulators) and issues tcgen05.mma; warps 2-5 read the accumulator (warp w
+// reads TMEM lanes 32*(w%4)..) and store the slab.  All waits are time-bounded
+// (sb_pipe.cuh).
 #include <cuda_bf16.h>
 
 #include <atomic>
@@ -38,11 +39,9 @@
 namespace sb {
 namespace {
 
-constexpr int kPThreads = 224;
-constexpr int kPProducerX = 6;                       // warp loading X
+constexpr int kPThreads = 192;
 constexpr uint32_t kPStageW = kTileA * kBlockK * 2;  // 16 KB of W per stage
 constexpr int kPMaxStages = 16;
-constexpr int kPStagesX = 4;
 constexpr int kPMaxGrid = 1024;
 
 struct PartialParams {
@@ -94,10 +93,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     uint8_t *sW = smem;
     uint8_t *sX = smem + p.stages_w * kPStageW;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sX + p.stages_x * x_bytes);
-    uint64_t *fullW = bars;
-    uint64_t *emptyW = bars + kPMaxStages;
-    uint64_t *fullX = bars + 2 * kPMaxStages;
-    uint64_t *emptyX = bars + 3 * kPMaxStages;
+    uint64_t *full = bars;                 // joint stage landed (W and X bytes)
+    uint64_t *empty = bars + kPMaxStages;  // joint stage consumed (one MMA commit)
     uint64_t *tfull = bars + 4 * kPMaxStages;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
@@ -112,12 +109,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages_w; ++i) {
-            mbar_init(&fullW[i], 1);
-            mbar_init(&emptyW[i], 1);
-        }
-        for (int i = 0; i < p.stages_x; ++i) {
-            mbar_init(&fullX[i], 1);
-            mbar_init(&emptyX[i], 1);
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
@@ -139,9 +132,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
     // The setup above touches no global memory, so it overlaps the previous kernel in the
     // stream (this kernel is a programmatic dependent launch).  W is a weight that kernel
-    // does not write, so ring W's first stages are filled before the wait (the W stream
-    // starts while the previous kernel finishes); X and the workspace may belong to that
-    // kernel, so everything else waits for it.
+    // does not write, so the first stages' W halves are loaded before the wait (the W stream
+    // starts while the previous kernel finishes; the expect covers the whole stage); X and
+    // the workspace may belong to that kernel, so everything else waits for it.
     uint32_t w_pre = 0;
     if (warp == 0 && lane == 0) {
         const uint32_t n = x_end - x_begin;
@@ -150,8 +143,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         int kb = static_cast<int>(x_begin) - tile * p.kb_tile;
         const uint64_t pol = policy_evict_first();
         for (uint32_t i = 0; i < w_pre; ++i) {
-            mbar_arrive_expect_tx(&fullW[i], kPStageW);
-            tma_load_2d(sW + i * kPStageW, &tmW, &fullW[i], kb * kBlockK, tile * kTileA, pol);
+            mbar_arrive_expect_tx(&full[i], kPStageW + x_bytes);
+            tma_load_2d(sW + i * kPStageW, &tmW, &full[i], kb * kBlockK, tile * kTileA, pol);
             if (++kb == p.kb_tile) {
                 kb = 0;
                 ++tile;
@@ -164,29 +157,24 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // this whole grid before it reads any slab
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    if (warp == 0 || warp == kPProducerX) {
-        if (lane == 0) {  // TMA producers: the CTA's K blocks in order, one ring each
-            const bool is_w = warp == 0;
-            const int stages = is_w ? p.stages_w : p.stages_x;
-            const uint32_t bytes = is_w ? kPStageW : x_bytes;
-            uint8_t *ring = is_w ? sW : sX;
-            uint64_t *full = is_w ? fullW : fullX;
-            uint64_t *empty = is_w ? emptyW : emptyX;
-            const CUtensorMap *tm = is_w ? &tmW : &tmX;
-            const uint64_t pol = is_w ? policy_evict_first() : policy_evict_last();
+    if (warp == 0) {
+        if (lane == 0) {  // TMA producer: the CTA's K blocks in order, W and X per stage
+            const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
             int stage = 0;
             uint32_t phase = 0, issued = 0;
             int tile = static_cast<int>(x_begin / p.kb_tile);
             int kb = static_cast<int>(x_begin) - tile * p.kb_tile;
             for (uint32_t x = x_begin; x < x_end; ++x) {
-                if (!(is_w && issued < w_pre)) {  // those were issued before the wait
+                const bool w_done = issued < w_pre;  // W issued (and expected) before the wait
+                if (!w_done) {
                     if (!bwait(&empty[stage], phase ^ 1u, wc)) break;
-                    mbar_arrive_expect_tx(&full[stage], bytes);
-                    tma_load_2d(ring + stage * bytes, tm, &full[stage], kb * kBlockK,
-                                is_w ? tile * kTileA : 0, pol);
+                    mbar_arrive_expect_tx(&full[stage], kPStageW + x_bytes);
+                    tma_load_2d(sW + stage * kPStageW, &tmW, &full[stage], kb * kBlockK,
+                                tile * kTileA, pol_w);
                 }
+                tma_load_2d(sX + stage * x_bytes, &tmX, &full[stage], kb * kBlockK, 0, pol_x);
                 ++issued;
-                if (++stage == stages) {
+                if (++stage == p.stages_w) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -195,15 +183,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     ++tile;
                 }
             }
-            const uint32_t n = issued < static_cast<uint32_t>(stages) ? issued : stages;
+            const uint32_t n = issued < static_cast<uint32_t>(p.stages_w) ? issued : p.stages_w;
             for (uint32_t i = issued - n; i < issued; ++i)
-                bwait_drain(&full[i % stages], (i / stages) & 1u, wc);
+                bwait_drain(&full[i % p.stages_w], (i / p.stages_w) & 1u, wc);
         }
     } else if (warp == 1) {
         if (lane == 0) {  // MMA issuer: one accumulation per piece
             const uint32_t idesc = idesc_bf16_f32(kTileA, p.nb);
-            int sw = 0, sx = 0, j = 0;
-            uint32_t pw = 0, px = 0;
+            int st = 0, j = 0;
+            uint32_t ph = 0;
             bool ok = true, any = false;
             uint32_t cut = first_cut;
             for (uint32_t x = x_begin; ok && x < x_end; ++j, cut += p.lane_kb) {
@@ -213,27 +201,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * p.nb);
                 for (uint32_t xx = x; xx < e; ++xx) {
-                    if (!bwait(&fullW[sw], pw, wc) || !bwait(&fullX[sx], px, wc)) {
+                    if (!bwait(&full[st], ph, wc)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t adesc = sw128_kmajor_desc(smem_u32(sW + sw * kPStageW));
-                    const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sX + sx * x_bytes));
+                    const uint64_t adesc = sw128_kmajor_desc(smem_u32(sW + st * kPStageW));
+                    const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sX + st * x_bytes));
 #pragma unroll
                     for (int ks = 0; ks < kBlockK / 16; ++ks)
                         umma_bf16(d_tmem, adesc + 2u * ks, bdesc + 2u * ks, idesc,
                                   (xx != x || ks != 0) ? 1u : 0u);
-                    umma_commit(&emptyW[sw]);
-                    umma_commit(&emptyX[sx]);
+                    umma_commit(&empty[st]);  // one commit frees the joint stage
                     any = true;
-                    if (++sw == p.stages_w) {
-                        sw = 0;
-                        pw ^= 1u;
-                    }
-                    if (++sx == p.stages_x) {
-                        sx = 0;
-                        px ^= 1u;
+                    if (++st == p.stages_w) {
+                        st = 0;
+                        ph ^= 1u;
                     }
                 }
                 if (ok) umma_commit(&tfull[b]);
@@ -438,10 +421,11 @@ int32_t sb_partial_completion(const void *X, const void *W, int64_t M, int64_t N
     p.pieces = pl.pieces;
     p.q = pl.q;
     p.r = pl.r;
-    p.stages_x = kPStagesX;
+    // joint stages (one K block of W and of X each), as many as fit
     p.stages_w = kPMaxStages;
-    while (p.stages_w > 2 && p_smem_bytes(p.nb, p.stages_w, p.stages_x) > kSmemLimit)
+    while (p.stages_w > 2 && p_smem_bytes(p.nb, p.stages_w, p.stages_w) > kSmemLimit)
         --p.stages_w;
+    p.stages_x = p.stages_w;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     p.epoch_word = reinterpret_cast<uint32_t *>(ws);
     p.status = reinterpret_cast<unsigned long long *>(ws + 8);
