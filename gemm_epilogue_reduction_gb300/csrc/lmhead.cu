@@ -11,11 +11,11 @@
 // Structure (the warp roles and TMEM epilogue of the "01 · 通算融合" note on Blackwell
 // SM100 GEMMs, sections 2 and 5.1: TMA producer, MMA issuer, epilogue warps; full-K
 // accumulation before any epilogue work):
-//   warps 0, 2  TMA producers (one lane each) of 64-wide K slices (128-byte swizzle).
-//               Vocab mode: one ring per operand, the ring of the operand streamed from HBM
-//               (W) deeper than the one re-read from L2 (H).  Rows mode: warp 0 alone fills
-//               one ring of joint stages (H rows and this CTA's half of the W tile), so the
-//               MMA waits on one barrier and commits once per K block;
+//   warp 0      the TMA producer (one lane) of 64-wide K slices (128-byte swizzle): one ring
+//               of joint stages, each holding one K block of both operands (vocab mode: 128
+//               W rows and all M rows of H; rows mode: 128 H rows and this CTA's half of the
+//               W tile), so the MMA waits on one barrier and commits once per K block (each
+//               commit costs the tensor pipe time); warp 2 has no role;
 //   warp 1      owns the TMEM allocation; one lane issues tcgen05.mma (M = 128, or
 //               M = 256 over a CTA pair in rows mode; bf16 x bf16 -> fp32) into one of two
 //               TMEM accumulators and commits stage releases and "accumulator full" to
@@ -628,8 +628,9 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
 }
 
 // ------------------------------------------------------------------ the kernel
-// Vocab mode: one producer per operand ring, so the operand streamed from HBM (W) can run
-// further ahead of the MMA than the one re-read from L2 (H).
+// Vocab mode with 16-row H blocks: one producer per operand ring, so that H (re-read from
+// L2, 2 KB per stage) takes 4 stages and W (streamed from HBM) every other stage that fits:
+// decode at 16 rows is bound by the W bytes in flight.
 __device__ __forceinline__ void produce_ring(const GemmParams &p, const CUtensorMap *tm,
                                              uint8_t *ring, uint32_t stage_bytes, int stages,
                                              uint64_t *full, uint64_t *empty, bool is_a,
@@ -656,6 +657,47 @@ __device__ __forceinline__ void produce_ring(const GemmParams &p, const CUtensor
             }
             mbar_arrive_expect_tx(&full[stage], stage_bytes);
             tma_load_2d(ring + stage * stage_bytes, tm, &full[stage], kb * kBlockK, row, policy);
+            ++issued;
+            if (++stage == stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    // Drain: the last `stages` issues may still be landing (only possible after an abort;
+    // on the normal path the MMA warp consumed every one of them).
+    const uint32_t n = issued < static_cast<uint32_t>(stages) ? issued : stages;
+    for (uint32_t i = issued - n; i < issued; ++i)
+        if (!bwait_drain(&full[i % stages], (i / stages) & 1u, abort_flag, p)) break;
+}
+
+// Vocab mode from 32 rows of H up: one ring of joint stages, each holding one K block of W
+// (128 vocabulary rows, operand A, 16 KB) and of H (all M rows, operand B); one thread loads
+// both, so the MMA warp waits once and commits once per K block.  The first `pre` stages' W copies (and their
+// expect) went out before the wait on the previous kernel; their H copies go out here.
+__device__ __forceinline__ void produce_vocab(const GemmParams &p, const CUtensorMap *tmA,
+                                              const CUtensorMap *tmB, uint8_t *sA, uint8_t *sB,
+                                              uint32_t b_bytes, uint64_t *full, uint64_t *empty,
+                                              int unit0, int unit_stride,
+                                              volatile int *abort_flag, uint32_t pre) {
+    const int stages = p.stages_a;
+    const uint64_t pol_w = policy_evict_first(), pol_h = policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0, issued = 0;
+    bool ok = true;
+    for (int tile = unit0; ok && tile < p.num_tiles; tile += unit_stride) {
+        const TileCoord c = tile_coord<true>(p, tile, 0);
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+            if (issued >= pre) {
+                if (!bwait(&empty[stage], phase ^ 1u, abort_flag, p)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[stage], kStageBytesA + b_bytes);
+                tma_load_2d(sA + stage * kStageBytesA, tmA, &full[stage], kb * kBlockK, c.a_row,
+                            pol_w);
+            }
+            tma_load_2d(sB + stage * b_bytes, tmB, &full[stage], kb * kBlockK, c.b_row, pol_h);
             ++issued;
             if (++stage == stages) {
                 stage = 0;
@@ -740,7 +782,9 @@ __device__ __forceinline__ void produce_pair(const GemmParams &p, const CUtensor
         if (!bwait_drain(&full[i % stages], (i / stages) & 1u, abort_flag, p)) break;
 }
 
-template <bool VOCAB, int EPI, int ATOMS>
+// ATOMS: rows mode, 64-wide K slices per joint stage.  JOINT: vocab mode, one joint ring
+// (otherwise one ring per operand).
+template <bool VOCAB, int EPI, int ATOMS, bool JOINT>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const GemmParams p, const uint32_t tmem_cols) {
@@ -826,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const TileCoord c = tile_coord<VOCAB>(p, unit0, rank);
         const uint64_t pol = policy_evict_first();
         for (uint32_t kb = 0; kb < a_pre; ++kb) {
-            mbar_arrive_expect_tx(&fullA[kb], kStageBytesA);
+            mbar_arrive_expect_tx(&fullA[kb], kStageBytesA + (JOINT ? b_stage_bytes : 0u));
             tma_load_2d(sA + kb * kStageBytesA, &tmA, &fullA[kb], static_cast<int>(kb) * kBlockK,
                         c.a_row, pol);
         }
@@ -874,15 +918,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0 || warp == 2) {
-        // ------------------------------------------------ TMA producers (one lane each).
-        // Vocab mode: warp 0 fills ring A (W, streamed once, evict first), warp 2 ring B (H,
-        // re-read from L2).  Rows mode: warp 0 fills the joint stages (H and the CTA's half
-        // of the W tile); warp 2 has no work.
+        // ------------------------------------------------ TMA producers (one lane each):
+        // warp 0 fills the joint stages (warp 2 then has no work), or, in vocab mode with
+        // separate rings, warp 0 ring A (W) and warp 2 ring B (H).
         if (lane == 0) {
             if (!VOCAB) {
                 if (warp == 0)
                     produce_pair<ATOMS>(p, &tmA, &tmB, sA, sB, b_stage_bytes, fullA, emptyA, rank,
                                  unit0, unit_stride, abort_flag, b_pre);
+            } else if (JOINT) {
+                if (warp == 0)
+                    produce_vocab(p, &tmA, &tmB, sA, sB, b_stage_bytes, fullA, emptyA, unit0,
+                                  unit_stride, abort_flag, a_pre);
             } else if (warp == 0) {
                 produce_ring(p, &tmA, sA, kStageBytesA, p.stages_a, fullA, emptyA, true,
                              policy_evict_first(), unit0, unit_stride, abort_flag, a_pre);
@@ -956,8 +1003,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (lane == 0) {
             // ------------------------------------------------ MMA issuer (one lane, vocab mode)
             const uint32_t idesc = idesc_bf16_f32(kTileA, p.nb);
-            int sa = 0, sb = 0;
-            uint32_t pa = 0, pb = 0;
+            int st = 0, sb = 0;
+            uint32_t ph = 0, pb = 0;
             bool ok = true, any = false;
             int it = 0;
             for (int tile = unit0; ok && tile < p.num_tiles; tile += unit_stride, ++it) {
@@ -967,26 +1014,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * p.nb);
                 for (int kb = 0; kb < p.kblocks; ++kb) {
-                    if (!bwait(&fullA[sa], pa, abort_flag, p) ||
-                        !bwait(&fullB[sb], pb, abort_flag, p)) {
+                    if (!bwait(&fullA[st], ph, abort_flag, p) ||
+                        (!JOINT && !bwait(&fullB[sb], pb, abort_flag, p))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + sa * kStageBytesA));
-                    const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + sb * b_stage_bytes));
+                    const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + st * kStageBytesA));
+                    const uint64_t bdesc =
+                        sw128_kmajor_desc(smem_u32(sB + (JOINT ? st : sb) * b_stage_bytes));
 #pragma unroll
                     for (int ks = 0; ks < kBlockK / 16; ++ks)
                         umma_bf16(d_tmem, adesc + 2u * ks, bdesc + 2u * ks, idesc,
                                   (kb | ks) != 0 ? 1u : 0u);
-                    umma_commit(&emptyA[sa]);
-                    umma_commit(&emptyB[sb]);
+                    umma_commit(&emptyA[st]);  // joint ring: frees the whole stage
+                    if (!JOINT) umma_commit(&emptyB[sb]);
                     any = true;
-                    if (++sa == p.stages_a) {
-                        sa = 0;
-                        pa ^= 1u;
+                    if (++st == p.stages_a) {
+                        st = 0;
+                        ph ^= 1u;
                     }
-                    if (++sb == p.stages_b) {
+                    if (!JOINT && ++sb == p.stages_b) {
                         sb = 0;
                         pb ^= 1u;
                     }
@@ -1041,11 +1089,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool VOCAB, int EPI, int ATOMS>
+template <bool VOCAB, int EPI, int ATOMS, bool JOINT>
 cudaError_t launch_t1(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p,
                      size_t smem, int num_sms, cudaStream_t stream) {
     constexpr int CS = VOCAB ? 1 : kRowsCluster;
-    auto kern = lmhead_kernel<VOCAB, EPI, ATOMS>;
+    auto kern = lmhead_kernel<VOCAB, EPI, ATOMS, JOINT>;
     // The shared-memory opt-in is per device; every launch asks for at most kSmemLimit.
     static std::atomic<uint64_t> opted_in{0};
     int dev = 0;
@@ -1102,15 +1150,21 @@ cudaError_t launch_t1(const CUtensorMap &tmA, const CUtensorMap &tmB, const Gemm
     return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p, cols);
 }
 
-// Rows mode: the kernel specialised for the call's atoms per joint stage (1 or 2).
+// The kernel specialised for the call's pipeline: rows mode, atoms per joint stage (1 or 2);
+// vocab mode, joint ring or one ring per operand.
 template <bool VOCAB, int EPI>
 cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p,
                      size_t smem, int num_sms, cudaStream_t stream) {
     if constexpr (!VOCAB) {
         if (p.atoms == kMaxPairAtoms)
-            return launch_t1<false, EPI, kMaxPairAtoms>(tmA, tmB, p, smem, num_sms, stream);
+            return launch_t1<false, EPI, kMaxPairAtoms, true>(tmA, tmB, p, smem, num_sms,
+                                                              stream);
+        return launch_t1<false, EPI, 1, true>(tmA, tmB, p, smem, num_sms, stream);
+    } else {
+        if (p.joint)
+            return launch_t1<true, EPI, 1, true>(tmA, tmB, p, smem, num_sms, stream);
+        return launch_t1<true, EPI, 1, false>(tmA, tmB, p, smem, num_sms, stream);
     }
-    return launch_t1<VOCAB, EPI, 1>(tmA, tmB, p, smem, num_sms, stream);
 }
 
 }  // namespace

@@ -193,27 +193,21 @@ int32_t check_outputs(const sb_outputs *out, int32_t surface, bool need_ws) {
     return SB_OK;
 }
 
-#ifndef SB_VOCAB_STAGES_B
-#define SB_VOCAB_STAGES_B 4
-#endif
-// Ring depths.  Vocab mode: the ring of the operand re-read from L2 (H) gets a fixed depth,
-// the ring of the operand streamed from HBM (W) every remaining stage that fits in shared
-// memory.  Rows mode: joint stages (this CTA's H rows and its half of the W tile for one K
-// block of `atoms` 64-wide slices), as many as fit.
-bool pick_stages(int nb, bool vm, int atoms, int flags, int topk, int *sa, int *sb) {
-    if (vm) {  // A = W (streamed), B = H
-        *sb = SB_VOCAB_STAGES_B;
-        for (*sa = kMaxStages; *sa > 1; --*sa)
-            if (lmhead_smem_bytes(nb, *sa, *sb, vm, flags, topk, 1) <= kSmemLimit) break;
-    } else {   // A = H, B = W half-tile, one joint ring
-        for (*sa = kMaxStages; *sa > 1; --*sa) {
-            *sb = *sa;
-            if (lmhead_smem_bytes(nb, *sa, *sb, vm, flags, topk, atoms) <= kSmemLimit) break;
-        }
-        *sb = *sa;
+// Ring depths.  Joint ring (rows mode; vocab mode from 32 rows of H): one K block of both
+// operands per stage (vocab mode: 128 W rows and all M rows of H; rows mode: this CTA's H
+// rows and its half of the W tile for `atoms` 64-wide slices), as many as fit.  Vocab mode at
+// 16 rows: one ring per operand, H a fixed depth and W every remaining stage (decode at
+// 16 rows is bound by the W bytes in flight, and H costs only 2 KB per stage).
+constexpr int kVocabStagesH = 4;
+bool pick_stages(int nb, bool vm, bool joint, int atoms, int flags, int topk, int *sa,
+                 int *sb) {
+    const int at = vm ? 1 : atoms;
+    for (*sa = kMaxStages; *sa > 1; --*sa) {
+        *sb = joint ? *sa : kVocabStagesH;
+        if (lmhead_smem_bytes(nb, *sa, *sb, vm, flags, topk, at) <= kSmemLimit) break;
     }
-    return lmhead_smem_bytes(nb, *sa, *sb, vm, flags, topk, vm ? 1 : atoms) <= kSmemLimit &&
-           *sa >= 2 && *sb >= 2;
+    *sb = joint ? *sa : kVocabStagesH;
+    return lmhead_smem_bytes(nb, *sa, *sb, vm, flags, topk, at) <= kSmemLimit && *sa >= 2;
 }
 
 CombineParams combine_params(const sb_outputs *out, const Workspace &w, int64_t M, int32_t k,
@@ -342,9 +336,10 @@ int32_t prepare(const void *H, const void *W, int64_t M, int64_t d, int64_t V, i
     // pairs, so that each W tile is shared by several pairs and the tensor pipe sets the pace;
     // one atom (7 joint stages, deeper buffering of the W stream) for a single pair of M tiles.
     p.atoms = (vm || p.m_groups < 2) ? 1 : kMaxPairAtoms;
+    p.joint = (!vm || p.nb >= 32) ? 1 : 0;
     const int64_t kb_cols = static_cast<int64_t>(p.atoms) * kBlockK;
     p.kblocks = static_cast<int>((d + kb_cols - 1) / kb_cols);
-    if (!pick_stages(p.nb, vm, p.atoms, flags, K, &p.stages_a, &p.stages_b))
+    if (!pick_stages(p.nb, vm, p.joint != 0, p.atoms, flags, K, &p.stages_a, &p.stages_b))
         return SB_ERR_UNSUPPORTED;
     p.flags = flags;
     p.topk = K;

@@ -69,6 +69,7 @@ struct GemmParams {
     int stages_a;          // ring depth of the UMMA A operand (16 KB stages)
     int stages_b;          // ring depth of the UMMA B operand (nb * 128 B stages)
     int atoms;             // rows mode: 64-wide K atoms per joint stage (1 or 2)
+    int joint;             // vocab mode: one joint ring (1) or one ring per operand (0)
     int flags;
     int topk;              // K of the top-K surface (0 otherwise)
     float inv_t;
