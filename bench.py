@@ -101,8 +101,8 @@ NOMINAL_PEAKS = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0}
 # null once the source differs.
 KERNEL_TRAFFIC = {
     # decode16: dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
-    # (1,556,172,288 + 2,995,456 B; W + H are 1,555,988,480 B).
-    "decode16": {"bytes": 1559167744, "src_sha": "82219ec0228f5a3d"},
+    # (1,556,144,640 + 3,022,336 B; W + H are 1,555,988,480 B).
+    "decode16": {"bytes": 1559166976, "src_sha": "1d6b3c04aa96dd72"},
 }
 
 
