@@ -47,3 +47,25 @@ def test_on_device_plans_of_this_library():
         assert d == 1, beta
     assert sb.sb_select_source_projection(1, 0, 0, 0, -1.0, 0, 0, 0)[0] == -1
     assert sb.sb_select_source_projection(math.nan, 0, 0, 0, 1.0, 0, 0, 0)[0] == -1
+
+
+def test_bench_plan_selection_on_given_costs():
+    """The benchmark's Equation (7) table (host logic, no GPU): payload bytes from the
+    library, the oracle's decision on every link, and the threshold link rate where both
+    sides meet (none when projecting costs no more on the device)."""
+    import bench
+    M, V, k = 64, 151936, 2
+    cheap = bench.plan_selection(M, V, k, 180e-6, 186e-6)   # projection faster locally
+    assert cheap["threshold_bytes_per_s"] is None
+    assert cheap["bytes_ref"] == 2 * M * V
+    assert cheap["bytes_proj"] == sb.sb_payload_bytes(M, k, sb.SB_TOKEN) == 12 * M * k
+    assert all(d["project"] == 1 for d in cheap["decisions"].values())
+    costly = bench.plan_selection(M, V, k, 200e-6, 186e-6)  # projection 14 us slower locally
+    thr = costly["threshold_bytes_per_s"]
+    assert thr == pytest.approx((costly["bytes_ref"] - costly["bytes_proj"]) / 14e-6)
+    for name, d in costly["decisions"].items():
+        od, om = oracle.select_source_projection(costly["bytes_ref"], costly["bytes_proj"],
+                                                 k, k, d["link_bytes_per_s"], 0.0, 200e-6,
+                                                 186e-6)
+        assert d["project"] == od and d["margin_s"] == om
+        assert od == (1 if d["link_bytes_per_s"] < thr else 0), name
