@@ -910,7 +910,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int t = p.targets[i];
             bad |= (t < 0 || t >= p.V);
         }
-        if (bad) atomicMax(p.ws.status, (static_cast<unsigned long long>(p.epoch) << 32) | 1ull);
+        if (bad) record_status(p.ws.status, p.epoch, 1u);  // SB_ERR_INVALID_ARG
     }
     if (VOCAB && (p.flags & kFlagTargets)) __syncthreads();  // tgt_s is complete
     // Let the record combine (a programmatic dependent launch) get scheduled early; it

@@ -11,7 +11,7 @@
 namespace sb {
 
 struct WaitCtx {
-    unsigned long long *status;  // (epoch << 32) | code, updated with atomicMax
+    unsigned long long *status;  // (epoch << 32) | code, updated with record_status
     uint32_t epoch;
     unsigned long long timeout_ns;
     volatile int *abort_flag;    // in shared memory
@@ -19,12 +19,32 @@ struct WaitCtx {
 
 constexpr uint32_t kTimeoutStatus = 6;  // SB_ERR_DEVICE_TIMEOUT
 
+// Records `code` for launch `epoch` in the status word (epoch << 32) | code.  The word sits
+// in caller memory that is never initialised, so it may hold anything: a word tagged with
+// another epoch is replaced, and within the same epoch (CUDA-graph replays reuse theirs) the
+// larger, i.e. worse, code is kept.
+static __device__ __noinline__ void record_status(unsigned long long *status, uint32_t epoch,
+                                                  uint32_t code) {
+    const unsigned long long mine = (static_cast<unsigned long long>(epoch) << 32) | code;
+    unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(status);
+    // each retry means another writer changed the word; a launch has only a few writers, so
+    // the bound is never reached
+    for (int tries = 0; tries < 4096; ++tries) {
+        const bool same = static_cast<uint32_t>(old >> 32) == epoch;
+        const unsigned long long want = (same && old > mine) ? old : mine;
+        if (want == old) return;
+        const unsigned long long seen = atomicCAS(status, old, want);
+        if (seen == old) return;
+        old = seen;
+    }
+}
+
 // Scalars by value: a context passed by reference to an out-of-line function would be kept
 // in local memory at every wait site.
 static __device__ __noinline__ void raise_timeout(unsigned long long *status, uint32_t epoch,
                                                   volatile int *abort_flag) {
     *abort_flag = 1;
-    atomicMax(status, (static_cast<unsigned long long>(epoch) << 32) | kTimeoutStatus);
+    record_status(status, epoch, kTimeoutStatus);
 }
 
 // Bounded wait on an mbarrier phase.  Returns false when the CTA is aborting (another role

@@ -140,11 +140,13 @@ def test_token_surface_leaves_a_logits_buffer_untouched():
     assert bool((sentinel == 12345).all())
 
 
-@pytest.mark.parametrize("M", [16, 300])
+@pytest.mark.parametrize("M", [16, 64, 200, 300])
 def test_device_watchdog_reports_timeout_and_context_survives(M):
     """A wait that nothing will satisfy runs out after the configured limit; the kernel
-    records SB_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, releases TMEM and exits (for
-    M = 300 inside 2-CTA clusters); the next call is correct."""
+    records SB_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, releases TMEM and exits (every
+    pipeline: one ring per operand at 16 rows, the joint ring at 64, CTA pairs with one K atom
+    per stage at 200 rows (one pair of M tiles) and with two at 300); the next call is
+    correct."""
     d, V, k = 128, 2048, 2
     H, W = synth.make_hw(M, d, V, seed=2)
     H, W = H.cuda(), W.cuda()
@@ -213,6 +215,28 @@ def test_topk_at_its_limits():
     res = sb.project(H, W, k, sb.SB_TOPK_LOGPROB, topk=K)
     torch.cuda.synchronize()
     check_topk(res, H, W, K)
+
+
+@pytest.mark.parametrize("M", [16, 300])
+def test_status_word_is_recorded_over_any_workspace_contents(M):
+    """The workspace needs no initialisation, so its status word may hold anything, even a
+    value larger than any status: a device-side error is still recorded for the launch that
+    raised it, and the next clean launch on the same bytes reads as OK."""
+    d, V, k = 64, 1000, 2
+    H, W = synth.make_hw(M, d, V, seed=6)
+    H, W = H.cuda(), W.cuda()
+    tg = synth.make_targets(M, V, device="cuda")
+    bad = tg.clone()
+    bad[M - 1] = V + 5
+    nbytes = sb.sb_workspace_bytes(M, V, k, sb.SB_TOKEN_LOGPROB)
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device="cuda")
+    res = sb.project(H, W, k, sb.SB_TOKEN_LOGPROB, targets=bad, workspace=ws)
+    torch.cuda.synchronize()
+    assert sb.sb_last_device_status(res["_outputs"]) == sb.SB_ERR_INVALID_ARG
+    ws.fill_(0xFF)
+    res = sb.project(H, W, k, sb.SB_TOKEN_LOGPROB, targets=tg, workspace=ws)
+    torch.cuda.synchronize()
+    assert sb.sb_last_device_status(res["_outputs"]) == sb.SB_OK
 
 
 @pytest.mark.parametrize("M", [16, 300])
