@@ -479,16 +479,17 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
     const int tgt = ((p.flags & kFlagTargets) && rv) ? __ldg(p.targets + row) : -1;
     float rm = -INFINITY, rs = 0.f, gk = -INFINITY, gz = 0.f;
     int ri = INT_MAX, gi = INT_MAX;
-    // top-K: a sorted list (largest first, equal values by ascending column) of the KL
-    // largest seen (KL >= K); only the first K are written
-    float tv[TOPK ? KL : 1];
-    int ti[TOPK ? KL : 1];
+    // top-K: a sorted list (largest first) of the KL largest keys seen (KL >= K); only the
+    // first K are written.  A key is the logit's order-preserving 32-bit image with its low
+    // 7 bits replaced by 127 - (column offset in the record): one unsigned compare orders
+    // by value, equal values by ascending column, and an insertion is one max and one min
+    // per entry.  The value read back (tag bits cleared) is within 127 units in the last
+    // place of the logit (8e-6 relative); values closer than that may order by column.
+    // Key 0 = empty.
+    uint32_t tk[TOPK ? KL : 1];
     if (TOPK) {
 #pragma unroll
-        for (int r = 0; r < KL; ++r) {
-            tv[r] = -INFINITY;
-            ti[r] = INT_MAX;
-        }
+        for (int r = 0; r < KL; ++r) tk[r] = 0u;
     }
     constexpr int kChunks = kRecordCols / 32;
 #pragma unroll 1
@@ -557,24 +558,20 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
             }
         }
         if (TOPK) {
-            // insertion without branches: entry r becomes the old entry r-1 if y beats it,
-            // else y if y beats entry r, else stays; a y that beats no entry changes nothing
-            // (invalid columns are -inf).  Columns arrive in ascending order, so an equal
-            // value already in the list has a lower column and stays ahead.
+            // insertion without branches: the key passes down the list, each entry keeping
+            // the larger of itself and the passing key (invalid columns, past the shard end,
+            // carry key 0 and change nothing)
+            const uint32_t tag0 = 127u - static_cast<uint32_t>(ch * 32);
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                const float x = y[j];
-                const int xc = cb + j;
-                bool gt[KL];
+                uint32_t x = (float_to_ordered(y[j]) & 0xFFFFFF80u) | (tag0 - j);
+                if (nval != 32) x = j < nval ? x : 0u;
 #pragma unroll
-                for (int r = 0; r < KL; ++r) gt[r] = x > tv[r];
-#pragma unroll
-                for (int r = KL - 1; r >= 1; --r) {
-                    tv[r] = gt[r - 1] ? tv[r - 1] : (gt[r] ? x : tv[r]);
-                    ti[r] = gt[r - 1] ? ti[r - 1] : (gt[r] ? xc : ti[r]);
+                for (int r = 0; r < KL; ++r) {
+                    const uint32_t hi = max(tk[r], x);
+                    x = min(tk[r], x);
+                    tk[r] = hi;
                 }
-                tv[0] = gt[0] ? x : tv[0];
-                ti[0] = gt[0] ? xc : ti[0];
             }
         }
         if (tgt >= cb && tgt < cb + nval) {
@@ -620,8 +617,12 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
 #pragma unroll
             for (int r = 0; r < KL; ++r) {
                 if (r >= p.topk) break;
-                p.ws.tkv[o * p.topk + r] = tv[r];
-                p.ws.tki[o * p.topk + r] = ti[r];
+                const uint32_t key = tk[r];
+                // the value without the column tag: equal logits of different records read
+                // back identical, so the combine's column tie-break orders them
+                p.ws.tkv[o * p.topk + r] = key ? ordered_to_float(key & 0xFFFFFF80u) : -INFINITY;
+                p.ws.tki[o * p.topk + r] =
+                    key ? cbase0 + 127 - static_cast<int>(key & 0x7Fu) : INT_MAX;
             }
         }
     }
