@@ -58,8 +58,11 @@ struct SmemLayout {
     uint32_t a_off, b_off, bar_off, misc_off, tgt_off, scratch_off, total;
 };
 
-// Shared memory: ring A (stages_a x 16 KB), ring B (stages_b x nb*128 B), mbarriers,
-// TMEM address + abort flag, vocab-mode target ids and cross-quadrant scratch.
+// Shared memory: the A halves of the stages (stages_a x atoms x 16 KB), the B halves
+// (stages_b x atoms x nb*128 B, half of that per CTA in rows mode), mbarriers, TMEM address
+// + abort flag, vocab-mode target ids and cross-quadrant scratch.  With a joint ring
+// stages_a == stages_b and stage s is the pair (A half s, B half s); with split rings the
+// two halves are independent rings of their own depths.
 __host__ __device__ inline SmemLayout make_layout(int nb, int stages_a, int stages_b, bool vocab,
                                                   int flags, int topk, int atoms) {
     SmemLayout L;
