@@ -61,6 +61,8 @@ WORKLOADS = {
                           desc="256-row batch, top-8 log-probs: H[256,5120] x W[151936,5120] bf16, k=4"),
     "sampling_token": dict(M=256, d=5120, V=151936, k=4, surface="token_logprob",
                            desc="256-row decode batch: H[256,5120] x W[151936,5120] bf16, k=4, TOKEN + log-prob"),
+    "sampling_full": dict(M=256, d=5120, V=151936, k=4, surface="full_logits",
+                          desc="256-row batch, full logits: H[256,5120] x W[151936,5120] bf16, k=4, FULL_LOGITS"),
     "mlp_down": dict(kind="partial", M=64, N=5120, K=17408, lanes=2,
                      desc="row-parallel MLP down projection: X[64,17408] x W[5120,17408] bf16, 2 lanes, partials summed, bf16 out"),
     "mlp_down8": dict(kind="partial", M=8, N=5120, K=17408, lanes=2,
@@ -86,6 +88,8 @@ WORKLOADS = {
                                  desc="profiling case: H[64,1024] x W[151936,1024] bf16, k=2, TOKEN_LOGPROB"),
     "sampling_topk_small": dict(M=256, d=1024, V=151936, k=4, surface="topk_logprob", topk=8,
                                 desc="profiling case: H[256,1024] x W[151936,1024] bf16, k=4, top-8"),
+    "sampling_full_small": dict(M=256, d=1024, V=151936, k=4, surface="full_logits",
+                                desc="profiling case: H[256,1024] x W[151936,1024] bf16, k=4, FULL_LOGITS"),
     "sampling_small": dict(M=256, d=1024, V=151936, k=4, surface="gumbel_token", T=0.7,
                            seed=1234,
                            desc="profiling case: H[256,1024] x W[151936,1024] bf16, k=4, GUMBEL"),
@@ -101,8 +105,8 @@ NOMINAL_PEAKS = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0}
 # null once the source differs.
 KERNEL_TRAFFIC = {
     # decode16: dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
-    # (1,556,144,640 + 3,022,336 B; W + H are 1,555,988,480 B).
-    "decode16": {"bytes": 1559166976, "src_sha": "1d6b3c04aa96dd72"},
+    # (1,556,126,464 + 3,343,360 B; W + H are 1,555,988,480 B).
+    "decode16": {"bytes": 1559469824, "src_sha": "74bdf7ccae6a18e5"},
 }
 
 
