@@ -588,17 +588,27 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
         }
         if (FULL && rv) {
             uint16_t *dst = p.logits + static_cast<size_t>(row) * p.V + cb;
-            if (nval == 32 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+            const uint32_t mis = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(dst)) & 31u;
+            if (nval == 32 && (mis & 15u) == 0) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     pk[j] = static_cast<uint32_t>(bf16_bits_rn(__uint_as_float(raw[2 * j]))) |
                             (static_cast<uint32_t>(bf16_bits_rn(__uint_as_float(raw[2 * j + 1])))
                              << 16);
-                uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+                if (mis == 0) {
+                    // the chunk's 64 bytes are two whole sectors: one 32-byte store each, so
+                    // no sector reaches L2 in two halves
+                    st_global_v8(dst, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+                    st_global_v8(dst + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14],
+                                 pk[15]);
+                } else {
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    for (int j = 0; j < 4; ++j)
+                        d4[j] =
+                            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                }
             } else {
 #pragma unroll
                 for (int j = 0; j < 32; ++j)

@@ -287,4 +287,14 @@ __device__ __forceinline__ float ordered_to_float(uint32_t o) {
     return __uint_as_float(u);
 }
 
+// One 32-byte global store per thread (a whole sector; 256-bit stores are new with sm_100).
+// dst must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *dst, uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3, uint32_t a4, uint32_t a5, uint32_t a6,
+                                             uint32_t a7) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a0),
+                 "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+                 : "memory");
+}
+
 }  // namespace sb
