@@ -116,3 +116,33 @@ def test_sampling_gumbel_token():
     ref = _oracle(H, W, k, rows, gumbel=True, temperature=np.float32(T).item(), seed=seed)
     check_rows(res, ref, rows, gumbel=True, T=np.float32(T).item(), seed=seed)
     _library_reference_check(H, W, res, T=np.float32(T).item(), lse_only=True)
+
+
+def test_rows_mode_full_logits_at_the_sampling_shape():
+    """M=256, d=5120, V=151936, k=4, FULL_LOGITS (rows mode: CTA pairs, each thread storing
+    whole 32-byte sectors of its row): every bf16 logit within the tolerance plus half a bf16
+    ulp of torch's fp32 product, the tokens those of TOKEN on the same inputs, and 32 rows
+    spread over the batch against the oracle element by element."""
+    M, d, V, k = 256, 5120, 151936, 4
+    H, W = synth.make_hw(M, d, V, seed=0, device="cuda")
+    full = sb.project(H, W, k, sb.SB_FULL_LOGITS)
+    tok = sb.project(H, W, k, sb.SB_TOKEN)
+    torch.cuda.synchronize()
+    assert sb.sb_last_device_status(full["_outputs"]) == sb.SB_OK
+    assert torch.equal(full["token"], tok["token"])
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        z = H.float() @ W.float().T
+        lg = full["logits"].float()
+        half_ulp = torch.exp2(torch.floor(torch.log2(z.abs().clamp_min(2.0 ** -126))) - 8)
+        assert bool(((lg - z).abs() <= TOL + half_ulp).all())
+        del z, lg
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    rows = list(range(0, M, 8))
+    ref = _oracle(H, W, k, rows)
+    check_rows(full, ref, rows)
+    lg = full["logits"][rows].float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(lg - ref["z"]) <= TOL + bf16_half_ulp(ref["z"]))
+    _library_reference_check(H, W, full)
