@@ -7,7 +7,6 @@ Tolerances (numbers on the N(0, 1) logit scale of the synthetic inputs):
   * bf16 logits: |gpu - z| <= 5e-3 + half a bf16 ulp of z (round-to-nearest of an fp32
     value within 5e-3 of z).
 """
-import math
 
 import numpy as np
 import torch
