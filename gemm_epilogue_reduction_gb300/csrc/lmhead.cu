@@ -726,6 +726,11 @@ __device__ __forceinline__ void produce_vocab(const GemmParams &p, const CUtenso
         if (!bwait_drain(&full[i % stages], (i / stages) & 1u, abort_flag, p)) break;
 }
 
+// Rows mode: the L2 policy of the W copies (kWEvictFirstGroups).
+__device__ __forceinline__ uint64_t rows_w_policy(const GemmParams &p) {
+    return p.m_groups <= kWEvictFirstGroups ? policy_evict_first() : policy_evict_normal();
+}
+
 // Rows mode (CTA pairs): one ring of joint stages, each holding this CTA's 128 H rows (A)
 // and its half of the W tile (B) for one K block of ATOMS 64-wide atoms (16 KB per atom and
 // operand); one thread per CTA loads both.  The leader's full barrier counts every
@@ -742,7 +747,7 @@ __device__ __forceinline__ void produce_pair(const GemmParams &p, const CUtensor
     const bool peer = rank == 1;
     const int stages = p.stages_a;
     const uint32_t a_stage = kStageBytesA * ATOMS, b_stage = b_atom * ATOMS;
-    const uint64_t pol_a = policy_evict_last(), pol_b = policy_evict_normal();
+    const uint64_t pol_a = policy_evict_last(), pol_b = rows_w_policy(p);
     int stage = 0;
     uint32_t phase = 0, issued = 0;
     bool ok = true;
@@ -896,7 +901,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (PAIR && warp == 0 && lane == 0 && unit0 < p.num_tiles) {
         b_pre = static_cast<uint32_t>(p.stages_a < p.kblocks ? p.stages_a : p.kblocks);
         const TileCoord c = tile_coord<VOCAB>(p, unit0, rank);
-        const uint64_t pol = policy_evict_normal();
+        const uint64_t pol = rows_w_policy(p);
         for (uint32_t kb = 0; kb < b_pre; ++kb) {
             uint8_t *dst = sB + kb * b_stage_bytes * ATOMS;
             if (rank == 0)

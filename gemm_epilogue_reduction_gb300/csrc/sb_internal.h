@@ -25,6 +25,12 @@ constexpr int kRowsCluster = 2;
 // of both operands; with 2 (K block 128) the MMA warp waits once and commits once per
 // 8 MMAs, with 1 more stages fit in shared memory
 constexpr int kMaxPairAtoms = 2;
+// rows mode: the L2 policy of W.  A W tile is read by the m_groups CTA pairs of its column
+// range at about the same time.  Up to this many pairs W is loaded evict-first (no pair reads
+// it again, and the space keeps H, loaded evict-last); beyond it the tile must stay in L2
+// until every pair has read it (measured: 1 to 4 pairs 1-6 % faster evict-first, 8 and 16
+// pairs 2-5 % slower)
+constexpr int kWEvictFirstGroups = 4;
 
 constexpr int kEpiWarps = 8;         // two epilogue warps per TMEM lane quadrant
 constexpr int kFirstEpiWarp = 3;     // warps 0 and 2 load, warp 1 issues MMAs + owns TMEM
