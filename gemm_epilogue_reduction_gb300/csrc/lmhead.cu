@@ -728,7 +728,7 @@ __device__ __forceinline__ void produce_vocab(const GemmParams &p, const CUtenso
 
 // Rows mode: the L2 policy of the W copies (kWEvictFirstGroups).
 __device__ __forceinline__ uint64_t rows_w_policy(const GemmParams &p) {
-    return p.m_groups <= kWEvictFirstGroups ? policy_evict_first() : policy_evict_normal();
+    return p.m_groups <= kWEvictFirstGroups ? policy_evict_first() : policy_evict_last();
 }
 
 // Rows mode (CTA pairs): one ring of joint stages, each holding this CTA's 128 H rows (A)

@@ -27,9 +27,10 @@ constexpr int kRowsCluster = 2;
 constexpr int kMaxPairAtoms = 2;
 // rows mode: the L2 policy of W.  A W tile is read by the m_groups CTA pairs of its column
 // range at about the same time.  Up to this many pairs W is loaded evict-first (no pair reads
-// it again, and the space keeps H, loaded evict-last); beyond it the tile must stay in L2
-// until every pair has read it (measured: 1 to 4 pairs 1-6 % faster evict-first, 8 and 16
-// pairs 2-5 % slower)
+// it again, and the space keeps H, loaded evict-last); beyond it W is loaded evict-last like
+// H, as the tile must stay in L2 until every pair has read it (measured: 1 to 4 pairs 1-6 %
+// faster evict-first than evict-normal, 8 and 16 pairs 2-5 % slower; at 8 and 16 pairs
+// evict-last 1-3 % faster than evict-normal)
 constexpr int kWEvictFirstGroups = 4;
 
 constexpr int kEpiWarps = 8;         // two epilogue warps per TMEM lane quadrant
