@@ -105,8 +105,8 @@ NOMINAL_PEAKS = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0}
 # null once the source differs.
 KERNEL_TRAFFIC = {
     # decode16: dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
-    # (1,556,158,464 + 2,976,512 B; W + H are 1,555,988,480 B).
-    "decode16": {"bytes": 1559134976, "src_sha": "08c776abb36f54bb"},
+    # (1,556,225,024 + 3,008,256 B; W + H are 1,555,988,480 B).
+    "decode16": {"bytes": 1559233280, "src_sha": "2790657b0e438601"},
 }
 
 
