@@ -39,9 +39,13 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+# w_layout: how the workload stores W (packed once with sb_pack_weights where that streams
+# faster: the d = 5120 decode and 256-row shapes; row-major for the 64-row shape, whose
+# full-logit surface streams 2.8 % slower packed and its token surface no faster, and for
+# prefill scoring, where the layout makes no difference)
 WORKLOADS = {
     "decode16": dict(M=16, d=5120, V=151936, k=4, surface="token_logprob",
-                     desc="decode token-only: H[16,5120] x W[151936,5120] bf16, k=4 shards of 37984, TOKEN + chosen log-prob"),
+                     w_layout="packed", desc="decode token-only: H[16,5120] x W[151936,5120] bf16, k=4 shards of 37984, TOKEN + chosen log-prob"),
     "decode64": dict(M=64, d=4096, V=151936, k=2, surface="full_logits",
                      desc="decode full-logit: H[64,4096] x W[151936,4096] bf16, k=2, FULL_LOGITS"),
     "prefill": dict(M=4096, d=6144, V=200064, k=4, surface="token_logprob", targets=True,
@@ -49,20 +53,20 @@ WORKLOADS = {
     "decode64_token": dict(M=64, d=4096, V=151936, k=2, surface="token_logprob",
                            desc="decode token-only at the full-logit shape: H[64,4096] x W[151936,4096] bf16, k=2"),
     "sampling": dict(M=256, d=5120, V=151936, k=4, surface="gumbel_token", T=0.7, seed=1234,
-                     desc="seeded sampling: H[256,5120] x W[151936,5120] bf16, k=4, GUMBEL_TOKEN T=0.7"),
+                     w_layout="packed", desc="seeded sampling: H[256,5120] x W[151936,5120] bf16, k=4, GUMBEL_TOKEN T=0.7"),
     "decode16_sample": dict(M=16, d=5120, V=151936, k=4, surface="gumbel_token", T=0.7,
                             seed=1234,
-                            desc="decode seeded sampling: H[16,5120] x W[151936,5120] bf16, k=4, GUMBEL_TOKEN T=0.7"),
+                            w_layout="packed", desc="decode seeded sampling: H[16,5120] x W[151936,5120] bf16, k=4, GUMBEL_TOKEN T=0.7"),
     "tiny": dict(M=4, d=256, V=4096, k=2, surface="token_logprob",
-                 desc="tiny: H[4,256] x W[4096,256] bf16, k=2"),
+                 w_layout="packed", desc="tiny: H[4,256] x W[4096,256] bf16, k=2"),
     "decode16_topk": dict(M=16, d=5120, V=151936, k=4, surface="topk_logprob", topk=8,
-                          desc="decode top-8 log-probs: H[16,5120] x W[151936,5120] bf16, k=4"),
+                          w_layout="packed", desc="decode top-8 log-probs: H[16,5120] x W[151936,5120] bf16, k=4"),
     "sampling_topk": dict(M=256, d=5120, V=151936, k=4, surface="topk_logprob", topk=8,
-                          desc="256-row batch, top-8 log-probs: H[256,5120] x W[151936,5120] bf16, k=4"),
+                          w_layout="packed", desc="256-row batch, top-8 log-probs: H[256,5120] x W[151936,5120] bf16, k=4"),
     "sampling_token": dict(M=256, d=5120, V=151936, k=4, surface="token_logprob",
-                           desc="256-row decode batch: H[256,5120] x W[151936,5120] bf16, k=4, TOKEN + log-prob"),
+                           w_layout="packed", desc="256-row decode batch: H[256,5120] x W[151936,5120] bf16, k=4, TOKEN + log-prob"),
     "sampling_full": dict(M=256, d=5120, V=151936, k=4, surface="full_logits",
-                          desc="256-row batch, full logits: H[256,5120] x W[151936,5120] bf16, k=4, FULL_LOGITS"),
+                          w_layout="packed", desc="256-row batch, full logits: H[256,5120] x W[151936,5120] bf16, k=4, FULL_LOGITS"),
     "mlp_down": dict(kind="partial", M=64, N=5120, K=17408, lanes=2,
                      desc="row-parallel MLP down projection: X[64,17408] x W[5120,17408] bf16, 2 lanes, partials summed, bf16 out"),
     "mlp_down8": dict(kind="partial", M=8, N=5120, K=17408, lanes=2,
@@ -326,6 +330,16 @@ def run_reference(args, cfg, world, rank):
     print(json.dumps(line), flush=True)
 
 
+# the layout of W the projection calls read (--w-layout): "row", "packed", or "auto" = the
+# workload's own choice (its "w_layout", else row-major)
+W_LAYOUT = {"layout": "auto"}
+
+
+def layout_for(cfg) -> str:
+    lay = W_LAYOUT["layout"]
+    return cfg.get("w_layout", "row") if lay == "auto" else lay
+
+
 def make_projection(cfg, rank=0):
     """Inputs (seed 0; targets seed 1; rank r > 0 draws its own rows), caller-owned outputs
     and the three step closures of one projection workload on the current device."""
@@ -344,9 +358,18 @@ def make_projection(cfg, rank=0):
                                     topk=cfg.get("topk", 0))
     w.tps = sb.sb_tiles_per_shard(M, V, k)
     w.stream = torch.cuda.current_stream()
+    # W as the calls read it: row-major, or packed once here (a model parameter is laid out
+    # when it is loaded, not per call)
+    w.layout = layout_for(cfg)
+    if w.layout == "packed":
+        w.Warg, w.wsurf = sb.pack_weights(w.W, k, w.stream), w.surface | sb.SB_W_PACKED
+        torch.cuda.synchronize()
+    else:
+        w.Warg, w.wsurf = w.W, w.surface
 
     def records():
-        st = sb.sb_lmhead_records(w.H, w.W, M, d, V, k, w.surface, w.T, w.gseed, w.out, w.stream)
+        st = sb.sb_lmhead_records(w.H, w.Warg, M, d, V, k, w.wsurf, w.T, w.gseed, w.out,
+                                  w.stream)
         if st != sb.SB_OK:
             raise sb.SbError(st, "sb_lmhead_records")
 
@@ -357,7 +380,8 @@ def make_projection(cfg, rank=0):
             raise sb.SbError(st, "sb_combine_shard_records")
 
     def project():
-        st = sb.sb_lmhead_project(w.H, w.W, M, d, V, k, w.surface, w.T, w.gseed, w.out, w.stream)
+        st = sb.sb_lmhead_project(w.H, w.Warg, M, d, V, k, w.wsurf, w.T, w.gseed, w.out,
+                                  w.stream)
         if st != sb.SB_OK:
             raise sb.SbError(st, "sb_lmhead_project")
 
@@ -440,7 +464,7 @@ def measure_workload(name, seconds, peaks, peak_src, gpu_index):
     gemm_ms, comb_ms = kernel_times(w, min(K, 200))
     roof = projection_roofline(w, gemm_ms, comb_ms, peaks, peak_src,
                                tensor_bound=name.startswith("prefill"))
-    entry = {"desc": cfg["desc"], "surface": cfg["surface"], "steps": K,
+    entry = {"desc": cfg["desc"], "surface": cfg["surface"], "w_layout": w.layout, "steps": K,
              "step_us": step_ms * 1e3, "rows_per_s": w.M / (step_ms * 1e-3),
              "gemm_us": gemm_ms * 1e3, "combine_us": comb_ms * 1e3,
              "bound": roof["bound"], "frac": roof["frac"], "achieved": roof["achieved"],
@@ -611,12 +635,16 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode16", choices=sorted(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--w-layout", default="auto", choices=["auto", "row", "packed"],
+                    help="W as the calls read it: row-major [V, d], or packed once before "
+                         "timing (sb_pack_weights, SB_W_PACKED); auto = the workload's layout")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--per-config-seconds", type=float, default=0.4,
                     help="device seconds of back-to-back steps per entry of the per_config "
                          "table (N = 1, default workload only; 0 leaves the table out)")
     args = ap.parse_args()
+    W_LAYOUT["layout"] = args.w_layout
     cfg = WORKLOADS[args.workload]
     world, rank, local = dist_env()
     args.warmup = max(args.warmup, 3)
@@ -642,8 +670,8 @@ def main():
     # each rank draws its own batch of rows (weak scaling) and the same W
     w = make_projection(cfg, rank)
     M, d, V, k = w.M, w.d, w.V, w.k
-    H, W, out, stream = w.H, w.W, w.out, w.stream
-    surface, T, gseed = w.surface, w.T, w.gseed
+    H, W, out, stream = w.H, w.Warg, w.out, w.stream
+    surface, T, gseed = w.wsurf, w.T, w.gseed
 
     for _ in range(args.warmup):
         w.project()
@@ -720,7 +748,8 @@ def main():
     value = job_rows_per_s(world, M, ms_per_step)
     peaks, peak_src = load_peaks()
     tr = KERNEL_TRAFFIC.get(args.workload)
-    traffic = tr["bytes"] if tr and tr.get("src_sha") == kernel_src_hash() else None
+    traffic = (tr["bytes"] if tr and tr.get("src_sha") == kernel_src_hash() and
+               tr.get("w_layout", "row") == w.layout else None)
     roof = projection_roofline(w, gemm_avg, comb_avg, peaks, peak_src,
                                tensor_bound=args.workload.startswith("prefill"), traffic=traffic)
 
@@ -746,7 +775,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": args.workload, "M": M, "d": d, "V": V, "k": k,
-                       "surface": cfg["surface"], "desc": cfg["desc"],
+                       "surface": cfg["surface"], "desc": cfg["desc"], "w_layout": w.layout,
                        "l2": ("inputs larger than L2 (W %.2f GB streamed every step)"
                               % (V * d * 2 / 1e9)) if flush is None else
                              ("inputs %.1f MB fit in L2: L2 flushed (2x L2 written) before "

@@ -16,6 +16,7 @@ import threading
 
 SB_TOKEN, SB_TOKEN_LOGPROB, SB_FULL_LOGITS, SB_GUMBEL_TOKEN, SB_TOPK_LOGPROB = 0, 1, 2, 3, 4
 SB_MAX_TOPK = 16
+SB_W_PACKED = 0x100  # layout flag OR'ed into `surface`: W is the packed copy (sb_pack_weights)
 SURFACES = {"token": SB_TOKEN, "token_logprob": SB_TOKEN_LOGPROB,
             "full_logits": SB_FULL_LOGITS, "gumbel_token": SB_GUMBEL_TOKEN,
             "topk_logprob": SB_TOPK_LOGPROB}
@@ -67,6 +68,10 @@ def lib():
         L.sb_workspace_bytes.restype = ctypes.c_size_t
         L.sb_tiles_per_shard.argtypes = [i64, i64, i32]
         L.sb_tiles_per_shard.restype = i32
+        L.sb_packed_weight_bytes.argtypes = [i64, i64, i32]
+        L.sb_packed_weight_bytes.restype = ctypes.c_size_t
+        L.sb_pack_weights.argtypes = [P, i64, i64, i32, P, ctypes.c_size_t, P]
+        L.sb_pack_weights.restype = i32
         L.sb_lmhead_project.argtypes = [P, P, i64, i64, i64, i32, i32, ctypes.c_float, u64,
                                         ctypes.POINTER(sb_outputs), P]
         L.sb_lmhead_project.restype = i32
@@ -146,6 +151,15 @@ def sb_workspace_bytes(M: int, V: int, k: int, surface: int) -> int:
 
 def sb_tiles_per_shard(M: int, V: int, k: int) -> int:
     return int(lib().sb_tiles_per_shard(M, V, k))
+
+
+def sb_packed_weight_bytes(V: int, d: int, k: int) -> int:
+    return int(lib().sb_packed_weight_bytes(V, d, k))
+
+
+def sb_pack_weights(W, V, d, k, W_packed, nbytes, stream=None) -> int:
+    return int(lib().sb_pack_weights(_ptr(W), V, d, k, _ptr(W_packed), nbytes,
+                                     _stream(stream)))
 
 
 def sb_lmhead_project(H, W, M, d, V, k, surface, temperature, seed, out: sb_outputs,
@@ -362,17 +376,50 @@ def make_outputs(M: int, V: int, k: int, surface: int, *, device="cuda", lse=Tru
     return out, bufs
 
 
+class PackedWeights:
+    """The packed copy of a [V, d] W for k lane shards (``buf``: a uint8 CUDA tensor), as
+    written by ``sb_pack_weights``; pass it as ``W`` to ``project``."""
+
+    def __init__(self, buf, V: int, d: int, k: int):
+        self.buf, self.V, self.d, self.k = buf, V, d, k
+
+    def data_ptr(self):
+        return self.buf.data_ptr()
+
+
+def pack_weights(W, k: int, stream=None) -> PackedWeights:
+    """Pack the row-major bf16 W [V, d] (CUDA tensor) for k lane shards; enqueued on
+    ``stream``."""
+    import torch
+    V, d = W.shape
+    nbytes = sb_packed_weight_bytes(V, d, k)
+    if nbytes == 0:
+        raise SbError(SB_ERR_INVALID_ARG, "sb_packed_weight_bytes")
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=W.device)
+    st = sb_pack_weights(W, V, d, k, buf, nbytes, stream)
+    if st != SB_OK:
+        raise SbError(st, "sb_pack_weights")
+    return PackedWeights(buf, V, d, k)
+
+
 def project(H, W, k: int, surface: int = SB_TOKEN_LOGPROB, *, temperature: float = 1.0,
             seed: int = 0, targets=None, stream=None, lse=True, logprob=True, workspace=None,
             topk: int = 0):
-    """Run one projection call on torch CUDA tensors H [M, d] and W [V, d] (bf16).
+    """Run one projection call on torch CUDA tensors H [M, d] and W [V, d] (bf16), or W a
+    ``PackedWeights`` of the same k (then the call reads the packed layout).
 
     Returns the dict of output tensors (token, token_logprob, lse, logits, target_logprob,
     workspace, as requested). Asynchronous on ``stream``; raises SbError on a bad status."""
     M, d = H.shape
-    V = W.shape[0]
-    out, bufs = make_outputs(M, V, k, surface, device=H.device, lse=lse, logprob=logprob,
-                             targets=targets, workspace=workspace, topk=topk)
+    if isinstance(W, PackedWeights):
+        if W.k != k or W.d != d:
+            raise SbError(SB_ERR_INVALID_ARG, "project: packed W of another shape")
+        V = W.V
+        surface |= SB_W_PACKED
+    else:
+        V = W.shape[0]
+    out, bufs = make_outputs(M, V, k, surface & ~SB_W_PACKED, device=H.device, lse=lse,
+                             logprob=logprob, targets=targets, workspace=workspace, topk=topk)
     st = sb_lmhead_project(H, W, M, d, V, k, surface, temperature, seed, out, stream)
     if st != SB_OK:
         raise SbError(st, "sb_lmhead_project")

@@ -642,6 +642,32 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams &p, const TileCoo
 }
 
 // ------------------------------------------------------------------ the kernel
+// One K block (the 64 columns from k0) of the 128 W rows from `row` (a tile of shard c.s):
+// from the row-major W through a 2-D map, or from the packed copy (sb_pack_weights: each
+// such box 16 KB contiguous in memory) through a 4-D map (element, row in the tile, K
+// block, tile of the packed layout).
+__device__ __forceinline__ int packed_tile(const GemmParams &p, const TileCoord &c, int row) {
+    return c.s * p.t128 + (row - c.s * p.S) / kTileA;
+}
+__device__ __forceinline__ void load_w_block(void *dst, const CUtensorMap *tm, uint64_t *bar,
+                                             const GemmParams &p, const TileCoord &c, int k0,
+                                             int row, uint64_t policy) {
+    if (p.packed)
+        tma_load_4d(dst, tm, bar, 0, 0, k0 / kBlockK, packed_tile(p, c, row), policy);
+    else
+        tma_load_2d(dst, tm, bar, k0, row, policy);
+}
+__device__ __forceinline__ void load_w_block_pair(void *dst, const CUtensorMap *tm,
+                                                  uint32_t bar_cluster, const GemmParams &p,
+                                                  const TileCoord &c, int k0, int row,
+                                                  uint64_t policy) {
+    if (p.packed)
+        tma_load_4d_pair(dst, tm, bar_cluster, 0, 0, k0 / kBlockK, packed_tile(p, c, row),
+                         policy);
+    else
+        tma_load_2d_pair(dst, tm, bar_cluster, k0, row, policy);
+}
+
 // Vocab mode with 16-row H blocks: one producer per operand ring, so that H (re-read from
 // L2, 2 KB per stage) takes 4 stages and W (streamed from HBM) every other stage that fits:
 // decode at 16 rows is bound by the W bytes in flight.
@@ -670,7 +696,12 @@ __device__ __forceinline__ void produce_ring(const GemmParams &p, const CUtensor
                 break;
             }
             mbar_arrive_expect_tx(&full[stage], stage_bytes);
-            tma_load_2d(ring + stage * stage_bytes, tm, &full[stage], kb * kBlockK, row, policy);
+            if (is_a)
+                load_w_block(ring + stage * stage_bytes, tm, &full[stage], p, c, kb * kBlockK,
+                             row, policy);
+            else
+                tma_load_2d(ring + stage * stage_bytes, tm, &full[stage], kb * kBlockK, row,
+                            policy);
             ++issued;
             if (++stage == stages) {
                 stage = 0;
@@ -708,8 +739,8 @@ __device__ __forceinline__ void produce_vocab(const GemmParams &p, const CUtenso
                     break;
                 }
                 mbar_arrive_expect_tx(&full[stage], kStageBytesA + b_bytes);
-                tma_load_2d(sA + stage * kStageBytesA, tmA, &full[stage], kb * kBlockK, c.a_row,
-                            pol_w);
+                load_w_block(sA + stage * kStageBytesA, tmA, &full[stage], p, c, kb * kBlockK,
+                             c.a_row, pol_w);
             }
             tma_load_2d(sB + stage * b_bytes, tmB, &full[stage], kb * kBlockK, c.b_row, pol_h);
             ++issued;
@@ -770,10 +801,13 @@ __device__ __forceinline__ void produce_pair(const GemmParams &p, const CUtensor
                 const int k0 = (kb * ATOMS + at) * kBlockK;  // past d: read as zeros
                 if (peer) {
                     tma_load_2d_pair(da + at * kStageBytesA, tmA, fb, k0, c.a_row, pol_a);
-                    if (!w_done) tma_load_2d_pair(db + at * b_atom, tmB, fb, k0, c.b_row, pol_b);
+                    if (!w_done)
+                        load_w_block_pair(db + at * b_atom, tmB, fb, p, c, k0, c.b_row, pol_b);
                 } else {
                     tma_load_2d(da + at * kStageBytesA, tmA, &full[stage], k0, c.a_row, pol_a);
-                    if (!w_done) tma_load_2d(db + at * b_atom, tmB, &full[stage], k0, c.b_row, pol_b);
+                    if (!w_done)
+                        load_w_block(db + at * b_atom, tmB, &full[stage], p, c, k0, c.b_row,
+                                     pol_b);
                 }
             }
             ++issued;
@@ -890,8 +924,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t pol = policy_evict_first();
         for (uint32_t kb = 0; kb < a_pre; ++kb) {
             mbar_arrive_expect_tx(&fullA[kb], kStageBytesA + (JOINT ? b_stage_bytes : 0u));
-            tma_load_2d(sA + kb * kStageBytesA, &tmA, &fullA[kb], static_cast<int>(kb) * kBlockK,
-                        c.a_row, pol);
+            load_w_block(sA + kb * kStageBytesA, &tmA, &fullA[kb], p, c,
+                         static_cast<int>(kb) * kBlockK, c.a_row, pol);
         }
     }
     // Rows mode with CTA pairs: the same for W, operand B, in both CTAs of the pair, into the
@@ -910,10 +944,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int at = 0; at < ATOMS; ++at) {
                 const int k0 = (static_cast<int>(kb) * ATOMS + at) * kBlockK;
                 if (rank == 0)
-                    tma_load_2d(dst + at * b_stage_bytes, &tmB, &fullA[kb], k0, c.b_row, pol);
+                    load_w_block(dst + at * b_stage_bytes, &tmB, &fullA[kb], p, c, k0, c.b_row,
+                                 pol);
                 else
-                    tma_load_2d_pair(dst + at * b_stage_bytes, &tmB, mapa_rank(&fullA[kb], 0),
-                                     k0, c.b_row, pol);
+                    load_w_block_pair(dst + at * b_stage_bytes, &tmB, mapa_rank(&fullA[kb], 0),
+                                      p, c, k0, c.b_row, pol);
             }
         }
     }
@@ -1186,7 +1221,35 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmP
     }
 }
 
+// The packed copy of W (layout in sb.h at sb_pack_weights): one thread per 16 bytes of the
+// packed buffer, zeros for the rows past a shard's end in its last tile and for the
+// columns past d in the last K block.
+__global__ void pack_weights_kernel(const uint4 *__restrict__ W, uint4 *__restrict__ P,
+                                    long long V, long long d, int k) {
+    const long long S = V / k, t128 = (S + kTileA - 1) / kTileA;
+    const long long kbs = (d + kBlockK - 1) / kBlockK, d8 = d / 8;
+    const long long n = static_cast<long long>(k) * t128 * kbs * kTileA * (kBlockK / 8);
+    for (long long o = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; o < n;
+         o += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long j8 = o % (kBlockK / 8);
+        const long long i = (o / (kBlockK / 8)) % kTileA;
+        const long long kb = (o / (kBlockK / 8 * kTileA)) % kbs;
+        const long long tile = o / (kBlockK / 8 * kTileA * kbs);
+        const long long s = tile / t128, t = tile % t128;
+        const long long r = t * kTileA + i;  // row within the shard
+        const long long c8 = kb * (kBlockK / 8) + j8;
+        P[o] = (r < S && c8 < d8) ? W[(s * S + r) * d8 + c8] : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_pack_weights(const void *W, void *P, long long V, long long d, int k,
+                                int num_sms, cudaStream_t stream) {
+    pack_weights_kernel<<<num_sms * 8, 256, 0, stream>>>(static_cast<const uint4 *>(W),
+                                                         static_cast<uint4 *>(P), V, d, k);
+    return cudaGetLastError();
+}
 
 size_t lmhead_smem_bytes(int nb, int stages_a, int stages_b, bool vocab_mode, int flags,
                          int topk, int atoms) {

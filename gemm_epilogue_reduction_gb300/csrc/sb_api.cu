@@ -112,6 +112,7 @@ struct MapCacheEntry {
     const void *base;
     int64_t rows, d;
     int box_rows;
+    int packed_k;  // 0: a 2-D map over a row-major matrix; k: the 4-D map of a packed W
     CUtensorMap map;
     bool used;
 };
@@ -126,7 +127,8 @@ bool make_map(CUtensorMap *tm, const void *base, int64_t rows, int64_t d, int bo
     {
         std::lock_guard<std::mutex> lock(g_map_mu);
         for (const auto &e : g_map_cache)
-            if (e.used && e.base == base && e.rows == rows && e.d == d && e.box_rows == box_rows) {
+            if (e.used && e.base == base && e.rows == rows && e.d == d &&
+                e.box_rows == box_rows && e.packed_k == 0) {
                 *tm = e.map;
                 return true;
             }
@@ -142,7 +144,47 @@ bool make_map(CUtensorMap *tm, const void *base, int64_t rows, int64_t d, int bo
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
     std::lock_guard<std::mutex> lock(g_map_mu);
-    g_map_cache[g_map_next] = MapCacheEntry{base, rows, d, box_rows, *tm, true};
+    g_map_cache[g_map_next] = MapCacheEntry{base, rows, d, box_rows, 0, *tm, true};
+    g_map_next = (g_map_next + 1) % kMapCache;
+    return true;
+}
+
+// The packed W layout of sb_pack_weights for V rows, d columns and k lane shards: tiles of
+// 128 rows (ceil(S / 128) per shard) x K blocks of 64 columns, each block 16 KB contiguous.
+int64_t packed_t128(int64_t V, int32_t k) { return (V / k + kTileA - 1) / kTileA; }
+int64_t packed_kblocks(int64_t d) { return (d + kBlockK - 1) / kBlockK; }
+size_t packed_bytes(int64_t V, int64_t d, int32_t k) {
+    return static_cast<size_t>(k) * packed_t128(V, k) * packed_kblocks(d) * kTileA * kBlockK * 2;
+}
+
+// 4-D map over a packed W: (element, row in the tile, K block, tile), boxes of one 16 KB
+// block, 128-byte swizzle (the same shared-memory image as a 64 x 128 box of the 2-D map).
+bool make_packed_map(CUtensorMap *tm, const void *base, int64_t V, int64_t d, int32_t k) {
+    {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        for (const auto &e : g_map_cache)
+            if (e.used && e.base == base && e.rows == V && e.d == d && e.packed_k == k) {
+                *tm = e.map;
+                return true;
+            }
+    }
+    auto enc = encoder();
+    if (!enc) return false;
+    const int64_t kbs = packed_kblocks(d);
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(kBlockK), static_cast<cuuint64_t>(kTileA),
+                          static_cast<cuuint64_t>(kbs),
+                          static_cast<cuuint64_t>(k * packed_t128(V, k))};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(kBlockK) * 2,
+                             static_cast<cuuint64_t>(kBlockK) * 2 * kTileA,
+                             static_cast<cuuint64_t>(kBlockK) * 2 * kTileA * kbs};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(kBlockK), static_cast<cuuint32_t>(kTileA), 1, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    if (enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    g_map_cache[g_map_next] = MapCacheEntry{base, V, d, kTileA, k, *tm, true};
     g_map_next = (g_map_next + 1) % kMapCache;
     return true;
 }
@@ -252,6 +294,7 @@ unsigned long long wait_limit_ns() { return g_timeout_ns.load(); }
 extern "C" {
 
 size_t sb_workspace_bytes(int64_t M, int64_t V, int32_t k, int32_t surface) {
+    surface &= ~SB_W_PACKED;  // the records do not depend on the layout of W
     if (!shape_ok(M, V, k) || surface < SB_TOKEN || surface > SB_TOPK_LOGPROB) return 0;
     return ws_layout(M, k, tiles_per_shard(M, V, k), surface == SB_GUMBEL_TOKEN,
                      surface == SB_TOPK_LOGPROB ? kMaxTopK : 0)
@@ -261,6 +304,25 @@ size_t sb_workspace_bytes(int64_t M, int64_t V, int32_t k, int32_t surface) {
 int32_t sb_tiles_per_shard(int64_t M, int64_t V, int32_t k) {
     if (!shape_ok(M, V, k)) return -1;
     return tiles_per_shard(M, V, k);
+}
+
+size_t sb_packed_weight_bytes(int64_t V, int64_t d, int32_t k) {
+    if (!shape_ok(1, V, k) || d < 8 || d > (int64_t(1) << 24) || d % 8 != 0) return 0;
+    return packed_bytes(V, d, k);
+}
+
+int32_t sb_pack_weights(const void *W, int64_t V, int64_t d, int32_t k, void *W_packed,
+                        size_t bytes, void *stream) {
+    if (!W || !W_packed || !shape_ok(1, V, k) || d < 8 || d > (int64_t(1) << 24))
+        return SB_ERR_INVALID_ARG;
+    if (d % 8 != 0 || !aligned(W, 16) || !aligned(W_packed, 16)) return SB_ERR_ALIGNMENT;
+    if (bytes < packed_bytes(V, d, k)) return SB_ERR_WORKSPACE_TOO_SMALL;
+    DevInfo dev;
+    if (int32_t e = current_device(&dev)) return e;
+    if (launch_pack_weights(W, W_packed, V, d, k, dev.sms, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return SB_ERR_CUDA;
+    return SB_OK;
 }
 
 }  // extern "C"
@@ -294,6 +356,8 @@ struct Prepared {
 int32_t prepare(const void *H, const void *W, int64_t M, int64_t d, int64_t V, int32_t k,
                 int32_t surface, float temperature, uint64_t seed, const sb_outputs *out,
                 Prepared *pr) {
+    const bool packed = (surface & SB_W_PACKED) != 0;
+    surface &= ~SB_W_PACKED;
     if (!H || !W || !shape_ok(M, V, k) || d < 8 || d > (int64_t(1) << 24) ||
         surface < SB_TOKEN || surface > SB_TOPK_LOGPROB)
         return SB_ERR_INVALID_ARG;
@@ -351,10 +415,15 @@ int32_t prepare(const void *H, const void *W, int64_t M, int64_t d, int64_t V, i
     p.timeout_ns = g_timeout_ns.load();
     p.debug_stall = g_debug_stall.load();
 
-    // rows mode: each CTA of a cluster loads 256 / cluster rows of the shared W tile
-    const bool ok = vm ? (make_map(&pr->tmA, W, V, d, kTileA) && make_map(&pr->tmB, H, M, d, p.nb))
-                       : (make_map(&pr->tmA, H, M, d, kTileA) &&
-                          make_map(&pr->tmB, W, V, d, kRowsTileN / p.cluster));
+    // rows mode: each CTA of a cluster loads 256 / cluster rows of the shared W tile; with a
+    // packed W every W box (128 rows, 64 columns) is one 16 KB block of the packed layout
+    p.packed = packed ? 1 : 0;
+    p.t128 = static_cast<int>(packed_t128(V, k));
+    CUtensorMap *wmap = vm ? &pr->tmA : &pr->tmB;
+    const bool ok =
+        (vm ? make_map(&pr->tmB, H, M, d, p.nb) : make_map(&pr->tmA, H, M, d, kTileA)) &&
+        (packed ? make_packed_map(wmap, W, V, d, k)
+                : make_map(wmap, W, V, d, vm ? kTileA : kRowsTileN / p.cluster));
     if (!ok) return SB_ERR_CUDA;
     pr->smem = lmhead_smem_bytes(p.nb, p.stages_a, p.stages_b, vm, flags, K, p.atoms);
     pr->sms = dev.sms;

@@ -77,6 +77,8 @@ struct GemmParams {
     int stages_b;          // ring depth of the UMMA B operand (nb * 128 B stages)
     int atoms;             // rows mode: 64-wide K atoms per joint stage (1 or 2)
     int joint;             // vocab mode: one joint ring (1) or one ring per operand (0)
+    int packed;            // W in the packed layout (tile-contiguous 16 KB boxes, 4-D map)
+    int t128;              // packed layout: 128-row tiles per shard
     int flags;
     int topk;              // K of the top-K surface (0 otherwise)
     float inv_t;
@@ -111,6 +113,9 @@ struct CombineParams {
 cudaError_t launch_lmhead(bool vocab_mode, const CUtensorMap &tmA, const CUtensorMap &tmB,
                           const GemmParams &p, size_t smem, int num_sms, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
+// The packed copy of W [V, d] for k lane shards (layout in sb.h, sb_pack_weights).
+cudaError_t launch_pack_weights(const void *W, void *P, long long V, long long d, int k,
+                                int num_sms, cudaStream_t stream);
 cudaError_t launch_pack(const Workspace &ws, int M, int k, int T, bool gumbel,
                         long long col_offset, void *payload, cudaStream_t stream);
 cudaError_t launch_merge_payload(const CombineParams &c, const void *payload,

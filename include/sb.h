@@ -58,6 +58,15 @@ typedef enum sb_surface {
 /* Largest K of the SB_TOPK_LOGPROB surface. */
 #define SB_MAX_TOPK 16
 
+/* Layout flag OR'ed into the `surface` argument of the calls that read W (sb_lmhead_project,
+ * sb_lmhead_records, sb_lmhead_project_from_host, sb_host_step_create,
+ * sb_lmhead_project_static_scratch): W points to the packed copy written by
+ * sb_pack_weights for the same V, d and k instead of the row-major [V, d] matrix.  The
+ * results are bit for bit those of the row-major call (the same operands reach the same
+ * MMAs); only the memory layout of W, and so how fast it streams, differs.
+ * sb_workspace_bytes ignores the flag; the other calls reject it. */
+#define SB_W_PACKED 0x100
+
 typedef enum sb_status {
     SB_OK = 0,
     SB_ERR_INVALID_ARG = 1,          /* a size, enum, pointer or temperature is out of range */
@@ -132,6 +141,28 @@ typedef struct sb_outputs {
 /* Bytes of workspace one call needs (for SB_TOPK_LOGPROB: with K = SB_MAX_TOPK, enough for
  * every K); 0 if the arguments are invalid. */
 size_t sb_workspace_bytes(int64_t M, int64_t V, int32_t k, int32_t surface);
+
+/*
+ * The packed layout of W for the calls with SB_W_PACKED: every (128-row tile, 64-column K
+ * block) box the kernels read is one contiguous 16 KB block, so each box is one linear
+ * stream of HBM reads instead of 128 rows of 128 bytes, 2d bytes apart.  With S = V/k,
+ * T128 = ceil(S / 128) tiles per shard and KB = ceil(d / 64) K blocks, element (r, c) of W
+ * (row r of shard s = r / S, i = (r - s*S) mod 128 in tile t = (r - s*S) / 128; column c in
+ * K block kb = c / 64 at j = c mod 64) is bf16 number
+ *     (((s * T128 + t) * KB + kb) * 128 + i) * 64 + j
+ * of the packed buffer; the rows past a shard's end in its last tile and the columns past d
+ * in the last K block are zero.  A weight is packed once (it is a model parameter) and then
+ * read by every call.
+ */
+/* Bytes of the packed copy of a [V, d] W for k lane shards: k * T128 * KB * 16384; 0 if the
+ * arguments are invalid (the same shape rules as sb_lmhead_project, d % 8 == 0). */
+size_t sb_packed_weight_bytes(int64_t V, int64_t d, int32_t k);
+/* Writes the packed copy of the row-major W [V, d] (device, bf16, 16-byte aligned) into
+ * W_packed (device, 16-byte aligned, `bytes` >= sb_packed_weight_bytes), enqueued on
+ * `stream`.  SB_ERR_WORKSPACE_TOO_SMALL if `bytes` is short, SB_ERR_ALIGNMENT for a
+ * misaligned pointer or d % 8 != 0. */
+int32_t sb_pack_weights(const void *W, int64_t V, int64_t d, int32_t k, void *W_packed,
+                        size_t bytes, void *stream);
 
 /* Records per (row, lane shard): T = ceil((V / k) / 128), one per 128 vocabulary columns;
  * -1 if the arguments are invalid.  (M is accepted for symmetry and does not change T.) */

@@ -59,6 +59,22 @@ def test_tiles_per_shard_and_workspace_layout():
         256 + 3 * al(4 * n) + 2 * al(4 * n * sb.SB_MAX_TOPK) + al(4 * M))
 
 
+def test_packed_weight_bytes_closed_form():
+    # k * ceil(S / 128) tiles of ceil(d / 64) K blocks of 128 x 64 bf16 (16 KB each)
+    def want(V, d, k):
+        return k * (-(-(V // k) // 128)) * (-(-d // 64)) * 16384
+    for V, d, k in [(151936, 5120, 4), (151936, 4096, 2), (200064, 6144, 4), (300, 136, 3),
+                    (21, 8, 7), (4096, 256, 1)]:
+        assert sb.sb_packed_weight_bytes(V, d, k) == want(V, d, k)
+    assert sb.sb_packed_weight_bytes(151936, 5120, 4) == 4 * 297 * 80 * 16384
+    assert sb.sb_packed_weight_bytes(4097, 256, 2) == 0   # V % k != 0
+    assert sb.sb_packed_weight_bytes(4096, 260, 2) == 0   # d % 8 != 0
+    assert sb.sb_packed_weight_bytes(4096, 256, 0) == 0
+    # the records do not depend on the layout of W
+    assert sb.sb_workspace_bytes(16, 151936, 4, sb.SB_TOKEN_LOGPROB | sb.SB_W_PACKED) == \
+        sb.sb_workspace_bytes(16, 151936, 4, sb.SB_TOKEN_LOGPROB)
+
+
 def test_status_strings():
     for code in range(7):
         assert sb.sb_status_string(code)
@@ -98,6 +114,8 @@ def _outputs(ws_bytes=1 << 20, **kw):
     (dict(surface=sb.SB_TOPK_LOGPROB, V=1024, k=256,
           out=dict(topk_ids=0x50000000, topk_logprob=0x60000000, topk=4)), sb.SB_ERR_INVALID_ARG),
     (dict(surface=5), sb.SB_ERR_INVALID_ARG),
+    (dict(surface=sb.SB_TOKEN | 0x200), sb.SB_ERR_INVALID_ARG),  # unknown layout flag
+    (dict(surface=sb.SB_W_PACKED | 5), sb.SB_ERR_INVALID_ARG),
 ])
 def test_invalid_arguments_are_rejected_before_any_launch(case, expect):
     args = dict(H=0x30000000, W=0x40000000, M=4, d=256, V=4096, k=2, surface=sb.SB_TOKEN,
