@@ -109,8 +109,9 @@ NOMINAL_PEAKS = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0}
 # null once the source differs.
 KERNEL_TRAFFIC = {
     # decode16: dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
-    # (1,556,225,024 + 3,008,256 B; W + H are 1,555,988,480 B).
-    "decode16": {"bytes": 1559233280, "src_sha": "2790657b0e438601"},
+    # with W packed (1,557,352,448 + 2,670,592 B; W + H are 1,555,988,480 B, and the packed
+    # W pads each shard's last 96-column tile to 128 rows, 1.3 MB more).
+    "decode16": {"bytes": 1560023040, "src_sha": "cafe303e71c1a23a", "w_layout": "packed"},
 }
 
 
@@ -670,7 +671,9 @@ def main():
     # each rank draws its own batch of rows (weak scaling) and the same W
     w = make_projection(cfg, rank)
     M, d, V, k = w.M, w.d, w.V, w.k
-    H, W, out, stream = w.H, w.Warg, w.out, w.stream
+    H, W, out, stream = w.H, w.W, w.out, w.stream
+    Wc = w.Warg  # W as the calls read it (row-major, or its packed copy)
+    w_layout = w.layout
     surface, T, gseed = w.wsurf, w.T, w.gseed
 
     for _ in range(args.warmup):
@@ -717,7 +720,7 @@ def main():
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(E):
-        st = sb.sb_lmhead_project_from_host(H_host, H_dev, W, M, d, V, k, surface, T, gseed,
+        st = sb.sb_lmhead_project_from_host(H_host, H_dev, Wc, M, d, V, k, surface, T, gseed,
                                             e2e_out, tok_host, lp_host, stream)
         if st != sb.SB_OK:
             raise sb.SbError(st, "sb_lmhead_project_from_host")
@@ -730,7 +733,7 @@ def main():
 
     # ---- the same step as a serving loop would run it: captured once (sb_host_step_*),
     # one graph launch and one stream wait per step
-    hstep = sb.HostStep(H_host, H_dev, W, M, d, V, k, surface, T, gseed, e2e_out, tok_host,
+    hstep = sb.HostStep(H_host, H_dev, Wc, M, d, V, k, surface, T, gseed, e2e_out, tok_host,
                         lp_host)
     for _ in range(3):
         hstep(stream)
@@ -749,7 +752,7 @@ def main():
     peaks, peak_src = load_peaks()
     tr = KERNEL_TRAFFIC.get(args.workload)
     traffic = (tr["bytes"] if tr and tr.get("src_sha") == kernel_src_hash() and
-               tr.get("w_layout", "row") == w.layout else None)
+               tr.get("w_layout", "row") == w_layout else None)
     roof = projection_roofline(w, gemm_avg, comb_avg, peaks, peak_src,
                                tensor_bound=args.workload.startswith("prefill"), traffic=traffic)
 
@@ -765,7 +768,7 @@ def main():
 
     per_cfg = None
     if world == 1 and args.workload == "decode16" and args.per_config_seconds > 0:
-        del w, H, W, out, H_dev, H_host
+        del w, H, W, Wc, out, H_dev, H_host
         torch.cuda.empty_cache()
         per_cfg = per_config_table(args.per_config_seconds, peaks, peak_src, local)
 
@@ -775,7 +778,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": args.workload, "M": M, "d": d, "V": V, "k": k,
-                       "surface": cfg["surface"], "desc": cfg["desc"], "w_layout": w.layout,
+                       "surface": cfg["surface"], "desc": cfg["desc"], "w_layout": w_layout,
                        "l2": ("inputs larger than L2 (W %.2f GB streamed every step)"
                               % (V * d * 2 / 1e9)) if flush is None else
                              ("inputs %.1f MB fit in L2: L2 flushed (2x L2 written) before "
