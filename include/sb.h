@@ -174,10 +174,11 @@ int32_t sb_tiles_per_shard(int64_t M, int64_t V, int32_t k);
  * `stream` -- the fused GEMM + record epilogue, then the record combine
  * (sb_combine_shard_records) -- with no host synchronisation.
  *   H          device bf16 [M, d] row-major (K-major), 16-byte aligned.
- *   W          device bf16 [V, d] row-major (the output-head weight), 16-byte aligned.
+ *   W          device bf16 [V, d] row-major (the output-head weight), 16-byte aligned; or,
+ *              with SB_W_PACKED in `surface`, its packed copy (sb_pack_weights, same k).
  *   M, d, V    M >= 1, d >= 8 with d % 8 == 0, V >= 1.
  *   k          number of contiguous lane shards, 1 <= k <= 1024 and V % k == 0.
- *   surface    an sb_surface.
+ *   surface    an sb_surface, optionally OR'ed with SB_W_PACKED.
  *   temperature  SB_GUMBEL_TOKEN: finite and > 0 (the key is z * (1/T) + g); ignored
  *              otherwise.
  *   seed       SB_GUMBEL_TOKEN: the SplitMix64 stream seed.  Column j of row r draws the
