@@ -131,6 +131,24 @@ int main(void) {
             free(hLp);
         }
     }
+    /* the same call on a packed copy of W gives the same bits */
+    {
+        const size_t pb = sb_packed_weight_bytes(V, d, (int32_t)k);
+        void *dWp = NULL;
+        CHECK(pb > 0 && cudaMalloc(&dWp, pb) == cudaSuccess);
+        CHECK(sb_pack_weights(dW, V, d, (int32_t)k, dWp, pb, NULL) == SB_OK);
+        CHECK(sb_lmhead_project(dH, dWp, M, d, V, (int32_t)k, SB_TOKEN_LOGPROB | SB_W_PACKED,
+                                1.0f, 0, &out, NULL) == SB_OK);
+        CHECK(cudaDeviceSynchronize() == cudaSuccess);
+        int32_t ptok[8];
+        float plp[8], plse[8];
+        CHECK(cudaMemcpy(ptok, dTok, M * 4, cudaMemcpyDeviceToHost) == cudaSuccess);
+        CHECK(cudaMemcpy(plp, dLp, M * 4, cudaMemcpyDeviceToHost) == cudaSuccess);
+        CHECK(cudaMemcpy(plse, dLse, M * 4, cudaMemcpyDeviceToHost) == cudaSuccess);
+        CHECK(memcmp(ptok, tok, M * 4) == 0 && memcmp(plp, lp, M * 4) == 0 &&
+              memcmp(plse, lse, M * 4) == 0);
+        cudaFree(dWp);
+    }
     /* invalid arguments are refused before anything runs */
     CHECK(sb_lmhead_project(dH, dW, M, d, V + 1, (int32_t)k, SB_TOKEN, 1.0f, 0, &out, NULL) ==
           SB_ERR_INVALID_ARG);
