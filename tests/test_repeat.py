@@ -18,6 +18,8 @@ def _built():
 
 
 @pytest.mark.parametrize("M,d,V,k,surface,calls", [
+    (512, 1024, 65536, 4, sb.SB_TOKEN_LOGPROB | sb.SB_W_PACKED, 200),  # packed W, rows mode
+    (16, 1024, 151936, 4, sb.SB_TOKEN_LOGPROB | sb.SB_W_PACKED, 200),  # packed W, decode
     (512, 1024, 65536, 4, sb.SB_TOKEN_LOGPROB, 300),   # rows mode, CTA pairs, 2 M pairs
     (300, 512, 32768, 2, sb.SB_GUMBEL_TOKEN, 300),     # rows mode, odd number of M tiles
     (16, 1024, 151936, 4, sb.SB_TOKEN_LOGPROB, 300),   # vocab mode, decode shape
@@ -28,10 +30,13 @@ def _built():
 ])
 def test_many_calls_give_identical_bits(M, d, V, k, surface, calls):
     H, W = synth.make_hw(M, d, V, seed=M + d, device="cuda")
-    topk = 8 if surface == sb.SB_TOPK_LOGPROB else 0
-    out, bufs = sb.make_outputs(M, V, k, surface, topk=topk)
-    T = 0.8 if surface == sb.SB_GUMBEL_TOKEN else 1.0
-    keys = ["token", "token_logprob", "lse"] + (["logits"] if surface == sb.SB_FULL_LOGITS else [])
+    if surface & sb.SB_W_PACKED:
+        W = sb.pack_weights(W, k)
+    base = surface & ~sb.SB_W_PACKED
+    topk = 8 if base == sb.SB_TOPK_LOGPROB else 0
+    out, bufs = sb.make_outputs(M, V, k, base, topk=topk)
+    T = 0.8 if base == sb.SB_GUMBEL_TOKEN else 1.0
+    keys = ["token", "token_logprob", "lse"] + (["logits"] if base == sb.SB_FULL_LOGITS else [])
     keys += ["topk_ids", "topk_logprob"] if topk else []
 
     def call():
