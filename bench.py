@@ -703,6 +703,30 @@ def main():
     # ---- per-kernel durations: each kernel alone, K launches, events around each launch
     gemm_avg, comb_avg = kernel_times(w, K)
 
+    # ---- the same steps on the row-major W, when the workload reads a packed one (reported
+    # beside the line's value, which is the packed layout's)
+    row_major = None
+    if w_layout == "packed":
+        def project_row():
+            st = sb.sb_lmhead_project(H, W, M, d, V, k, w.surface, T, gseed, out, stream)
+            if st != sb.SB_OK:
+                raise sb.SbError(st, "sb_lmhead_project")
+        for _ in range(3):
+            project_row()
+        torch.cuda.synchronize()
+        row_ms = max_over_ranks(timed_steps(project_row, K, stream, flush), "cuda")
+        def records_row():
+            st = sb.sb_lmhead_records(H, W, M, d, V, k, w.surface, T, gseed, out, stream)
+            if st != sb.SB_OK:
+                raise sb.SbError(st, "sb_lmhead_records")
+        import types
+        row_gemm, _ = kernel_times(types.SimpleNamespace(records=records_row, combine=w.combine,
+                                                         stream=stream), min(K, 200))
+        row_major = {"ms_per_step": row_ms, "value": job_rows_per_s(world, M, row_ms),
+                     "unit": "rows/s", "kernel_ms": row_gemm,
+                     "frac": (V * d * 2 + M * d * 2 + 12 * M) / (row_gemm * 1e-3) /
+                             (load_peaks()[0]["hbm_gbs"] * 1e9)}
+
     # ---- end to end through the public call with host buffers: H is copied from pinned
     # host memory and token + log-prob are copied back inside the call, every step
     # (token and log-prob back to back on both sides, so they come back in one copy)
@@ -794,6 +818,7 @@ def main():
                               "api": "sb_host_step_create once, sb_host_step_launch per step"},
             "clocks": clocks.summary(),
             "gpu_launches": 2 * K,
+            "row_major_w": row_major,
             "wall_s_timed": t_wall,
             "per_config": per_cfg,
         }
